@@ -1,0 +1,209 @@
+/*
+ * pagedkv.h - C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * The library implements the attention layer's hot path of a vLLM-style
+ * engine as described in "Inside vLLM: Anatomy of a High-Throughput LLM
+ * Inference System" (page 1 unless noted):
+ *
+ *   paged_slot_mapping  - the slot_mapping built in "prepare inputs"
+ *                         ("Run forward pass", step 2);
+ *   paged_kv_write      - the forward pass populating the new tokens' KVs in
+ *                         paged KV memory ("Prefix Caching", populate-KV
+ *                         figure text);
+ *   paged_attention     - attention of every sequence over only its own
+ *                         tokens in one flattened "super sequence", reading
+ *                         K/V through per-request block tables ("Run forward
+ *                         pass", step 3), for decode tokens and chunked-
+ *                         prefill chunks in the same batch ("Scheduler": V1
+ *                         mixes prefill and decode in one step; "Chunked
+ *                         prefill"), with prefix-cached requests sharing
+ *                         physical blocks ("Prefix Caching").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All array arguments are DEVICE pointers owned by the caller. The
+ *    library allocates no device memory and keeps no per-call state; the
+ *    caller provides the attention workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every call only enqueues work on that stream and returns; the
+ *    outputs are ready when the stream reaches that point.
+ *  - bf16 tensors are row-major with the innermost dimension contiguous and
+ *    must start on a 16-byte boundary. int32 arrays need 4-byte alignment.
+ *  - The return value is PKV_OK or a negative PKV_E_* code. Argument errors
+ *    are detected on the host before anything is enqueued. Bad METADATA
+ *    (values inside device arrays, which the host never reads) is detected
+ *    by the kernels: they skip the offending entry, never access memory out
+ *    of bounds, and OR a PKV_DEV_* bit into a device status word that
+ *    pkv_read_status() fetches.
+ *  - Block size is fixed at 16 tokens ("Scheduler", allocate_slots: each
+ *    block stores 16 tokens by default).
+ *
+ * KV-cache layout
+ * ---------------
+ *  One bf16 tensor per layer, [num_blocks][2][num_kv_heads][16][head_size]:
+ *  index 0 of the second dimension holds K, index 1 holds V. One block is
+ *  one contiguous run of 2 * 16 * num_kv_heads * head_size * 2 bytes, the
+ *  per-block size the pages give (page 2, "LLM Engine 构造函数", KV-cache
+ *  manager note). Token slot s lives in block s / 16, row s % 16.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_BLOCK_SIZE 16
+
+/* Return codes. */
+#define PKV_OK 0
+#define PKV_E_NULL (-1)        /* a required pointer is NULL */
+#define PKV_E_DIMS (-2)        /* a size or count is out of range */
+#define PKV_E_GQA (-3)         /* num_q_heads is not a positive multiple of num_kv_heads */
+#define PKV_E_BLOCK_SIZE (-4)  /* block_size != 16 */
+#define PKV_E_HEAD_SIZE (-5)   /* head_size unsupported (attention: 64 or 128; KV write: multiple of 8) */
+#define PKV_E_WORKSPACE (-6)   /* workspace smaller than paged_attention_workspace_bytes() requires */
+#define PKV_E_ALIGN (-7)       /* a pointer is not aligned as required */
+#define PKV_E_CUDA (-8)        /* a CUDA runtime call or kernel launch failed */
+#define PKV_E_DEVICE (-9)      /* the device status word holds PKV_DEV_* bits */
+
+/* Bits of the device status word (OR-ed in by the kernels). */
+#define PKV_DEV_BAD_QSL 0x1      /* query_start_loc not ragged offsets 0 = qsl[0] <= ... <= qsl[R] = T */
+#define PKV_DEV_BAD_LEN 0x2      /* a request has new tokens > seq_len, or seq_len > 16 * max_blocks_per_req */
+#define PKV_DEV_BAD_BLOCK 0x4    /* a block_table entry that is read lies outside [0, num_blocks) */
+#define PKV_DEV_BAD_SLOT 0x8     /* a slot_mapping entry lies at or beyond 16 * num_blocks */
+#define PKV_DEV_TIMEOUT 0x10     /* an internal pipeline wait gave up (never expected) */
+#define PKV_DEV_OVERFLOW 0x20    /* internal work list overflow (never expected) */
+
+typedef struct {
+    int32_t num_blocks;    /* blocks in the pool */
+    int32_t block_size;    /* must be 16 */
+    int32_t num_kv_heads;
+    int32_t head_size;
+} pkv_cache_desc;
+
+/*
+ * Bytes of the whole KV pool of one layer: num_blocks * 2 * 16 *
+ * num_kv_heads * head_size * 2 (page 2 block-size note, bf16). Host only.
+ */
+int pkv_kv_cache_bytes(const pkv_cache_desc *desc, size_t *bytes);
+
+/*
+ * slot_mapping[t] for every new token t of a flattened batch ("Run forward
+ * pass", step 2). Request r owns tokens query_start_loc[r] ..
+ * query_start_loc[r+1]-1; with L = seq_lens[r] (context length including
+ * this step's tokens) and n its new-token count, token i of the request sits
+ * at position p = L - n + i and goes to slot
+ *     block_table[r][p / 16] * 16 + p % 16.
+ *
+ *  block_table      int32 [num_reqs][max_blocks_per_req]
+ *  seq_lens         int32 [num_reqs]
+ *  query_start_loc  int32 [num_reqs + 1]
+ *  slot_mapping     int32 [num_tokens] (output). A token whose request has
+ *                   bad metadata, or whose block id is outside the pool,
+ *                   gets -1 (which paged_kv_write skips) and raises a
+ *                   status bit.
+ *  status           optional device int32 (may be NULL); PKV_DEV_* bits are
+ *                   OR-ed in, never cleared.
+ */
+int paged_slot_mapping(const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                       const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_tokens,
+                       int32_t num_blocks, int32_t *slot_mapping, int32_t *status, void *stream);
+
+/*
+ * Scatters this step's K and V into the pool ("Prefix Caching": the forward
+ * pass populates the KVs in paged memory). For token t with slot s >= 0 and
+ * every kv head h:
+ *     kv_cache[s/16][0][h][s%16][:] = k[t][h][:]
+ *     kv_cache[s/16][1][h][s%16][:] = v[t][h][:]
+ * A negative slot is skipped (padding). A slot >= 16 * num_blocks is skipped
+ * and raises PKV_DEV_BAD_SLOT. Slots must be distinct within one call, and
+ * no block shared by several requests (a prefix-cache hit) may be a target.
+ *
+ *  k, v       bf16 [num_tokens][num_kv_heads][head_size]
+ *  kv_cache   bf16 pool, layout above; head_size a multiple of 8
+ */
+int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
+                   void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream);
+
+/*
+ * Workspace bytes paged_attention needs for batches of at most
+ * max_num_reqs requests and max_num_tokens new tokens on the current
+ * device. A smaller workspace (down to the size for max_num_reqs and
+ * max_num_tokens with no room for split-KV partials) still works: the
+ * library then splits long contexts less, or not at all.
+ */
+int paged_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens, int32_t num_q_heads,
+                                    const pkv_cache_desc *desc, size_t *bytes);
+
+/*
+ * The smallest workspace paged_attention accepts for those bounds: room for
+ * the work list but none for split-KV partials, so every (request, kv head,
+ * 16-row tile) is processed by one CTA over its whole context. Host only.
+ */
+int paged_attention_min_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens, int32_t num_q_heads,
+                                        const pkv_cache_desc *desc, size_t *bytes);
+
+/*
+ * Causal GQA attention of a flattened ragged batch over the paged pool
+ * ("Run forward pass", step 3). For new token t of request r (token i of
+ * the request, position p = L - n + i) and query head hq:
+ *
+ *   out[t][hq][:] = sum_{j=0..p} softmax_j(scale * q[t][hq] . K_r[j]) V_r[j]
+ *
+ * where K_r[j] / V_r[j] are row j % 16 of kv head hq / (num_q_heads /
+ * num_kv_heads) in block block_table[r][j / 16]. Decode tokens (n = 1),
+ * speculative/multi-token queries and chunked-prefill chunks (any n <= L)
+ * mix freely in one call. Call it after paged_kv_write of the same step, on
+ * the same stream. Long contexts are split across CTAs (split-KV) and
+ * merged with a log-sum-exp weighted reduction.
+ *
+ *  q          bf16 [num_tokens][num_q_heads][head_size], head_size 64 or 128
+ *  kv_cache   bf16 pool (read only)
+ *  out        bf16 [num_tokens][num_q_heads][head_size]; rows of requests
+ *             with bad metadata are left unwritten
+ *  workspace  device scratch of workspace_bytes bytes, 256-byte aligned;
+ *             its first 4 bytes are this call's device status word (cleared
+ *             at the start of the call). Calls that run concurrently need
+ *             separate workspaces.
+ */
+int paged_attention(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                    const void *kv_cache, const pkv_cache_desc *desc,
+                    const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                    const int32_t *seq_lens, const int32_t *query_start_loc,
+                    float scale, void *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attention, plus CUDA events recorded on `stream` between its
+ * launches, for measuring each kernel on the stream it runs on: events[0]
+ * before the work-list kernel, events[1] before the attention kernel,
+ * events[2] after it (before the split merge), events[3] after the merge.
+ * `events` holds four cudaEvent_t handles created by the caller (a NULL
+ * entry is skipped). Same arguments, results and errors as paged_attention.
+ */
+int paged_attention_timed(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                          const void *kv_cache, const pkv_cache_desc *desc,
+                          const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                          const int32_t *seq_lens, const int32_t *query_start_loc,
+                          float scale, void *out, void *workspace, size_t workspace_bytes, void *stream,
+                          void *const *events);
+
+/*
+ * Copies a device status word to *host_status after the work queued on
+ * `stream` so far has finished (synchronises the stream). Returns PKV_OK if
+ * the word is 0, PKV_E_DEVICE if bits are set, PKV_E_CUDA on a CUDA error.
+ * For paged_attention, pass the workspace pointer (its status word).
+ */
+int pkv_read_status(const int32_t *status, void *stream, int32_t *host_status);
+
+/* A static English description of a return code. */
+const char *pkv_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

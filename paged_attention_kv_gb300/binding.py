@@ -1,0 +1,281 @@
+"""Thin Python binding over ``libpagedkv.so`` (C ABI in ``include/pagedkv.h``).
+
+Argument marshalling only: each function checks that the torch tensors it is
+handed have the dtype, shape, device and contiguity the C call documents,
+passes their device pointers and the current CUDA stream, and raises
+``PagedKVError`` on a non-zero return code. Every step of the computation
+runs in the library's CUDA kernels; there is no other code path. If the
+library has not been built, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+BLOCK_SIZE = 16
+
+# Return codes and device status bits (pagedkv.h).
+PKV_OK = 0
+PKV_E_NULL = -1
+PKV_E_DIMS = -2
+PKV_E_GQA = -3
+PKV_E_BLOCK_SIZE = -4
+PKV_E_HEAD_SIZE = -5
+PKV_E_WORKSPACE = -6
+PKV_E_ALIGN = -7
+PKV_E_CUDA = -8
+PKV_E_DEVICE = -9
+PKV_DEV_BAD_QSL = 0x1
+PKV_DEV_BAD_LEN = 0x2
+PKV_DEV_BAD_BLOCK = 0x4
+PKV_DEV_BAD_SLOT = 0x8
+PKV_DEV_TIMEOUT = 0x10
+PKV_DEV_OVERFLOW = 0x20
+
+EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_attention_workspace_bytes",
+            "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed", "pkv_read_status",
+            "pkv_status_string")
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_size", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    desc_p = ctypes.POINTER(CacheDesc)
+    lib.pkv_kv_cache_bytes.argtypes = [desc_p, ctypes.POINTER(sz)]
+    lib.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+    lib.paged_kv_write.argtypes = [vp, vp, vp, i32, vp, desc_p, vp, vp]
+    lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
+    lib.paged_attention_min_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
+    lib.paged_attention.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+    lib.paged_attention_timed.argtypes = lib.paged_attention.argtypes + [ctypes.POINTER(vp)]
+    lib.pkv_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    for name in EXPORTED[:-1]:
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+LIB = _load()
+
+
+def status_string(code: int) -> str:
+    return LIB.pkv_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != PKV_OK:
+        raise PagedKVError(rc, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _want(t: torch.Tensor, dtype, ndim, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def cache_desc(kv_cache: torch.Tensor) -> CacheDesc:
+    """Descriptor of a pool tensor bf16 [num_blocks][2][num_kv_heads][16][head_size]."""
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2:
+        raise ValueError(f"kv_cache must be [num_blocks][2][num_kv_heads][16][head_size], got {tuple(kv_cache.shape)}")
+    nb, _, hkv, bs, d = kv_cache.shape
+    return CacheDesc(nb, bs, hkv, d)
+
+
+def pkv_kv_cache_bytes(num_blocks: int, num_kv_heads: int, head_size: int, block_size: int = BLOCK_SIZE) -> int:
+    out = ctypes.c_size_t(0)
+    _check(LIB.pkv_kv_cache_bytes(ctypes.byref(CacheDesc(num_blocks, block_size, num_kv_heads, head_size)),
+                                  ctypes.byref(out)), "pkv_kv_cache_bytes")
+    return out.value
+
+
+def paged_slot_mapping(block_table, seq_lens, query_start_loc, num_tokens: int, num_blocks: int,
+                       slot_mapping=None, status=None, stream=None) -> torch.Tensor:
+    _want(block_table, torch.int32, 2, "block_table")
+    _want(seq_lens, torch.int32, 1, "seq_lens")
+    _want(query_start_loc, torch.int32, 1, "query_start_loc")
+    num_reqs = seq_lens.shape[0]
+    if query_start_loc.shape[0] != num_reqs + 1 or block_table.shape[0] != num_reqs:
+        raise ValueError("block_table, seq_lens and query_start_loc disagree on the number of requests")
+    if slot_mapping is None:
+        slot_mapping = torch.empty(num_tokens, dtype=torch.int32, device=seq_lens.device)
+    _want(slot_mapping, torch.int32, 1, "slot_mapping")
+    if slot_mapping.shape[0] < num_tokens:
+        raise ValueError("slot_mapping is shorter than num_tokens")
+    _check(LIB.paged_slot_mapping(_ptr(block_table), num_reqs, block_table.shape[1], _ptr(seq_lens),
+                                  _ptr(query_start_loc), num_tokens, num_blocks, _ptr(slot_mapping), _ptr(status),
+                                  _stream(stream)), "paged_slot_mapping")
+    return slot_mapping
+
+
+def paged_kv_write(k, v, slot_mapping, kv_cache, status=None, stream=None) -> None:
+    _want(k, torch.bfloat16, 3, "k")
+    _want(v, torch.bfloat16, 3, "v")
+    _want(slot_mapping, torch.int32, 1, "slot_mapping")
+    _want(kv_cache, torch.bfloat16, 5, "kv_cache")
+    desc = cache_desc(kv_cache)
+    t = k.shape[0]
+    if v.shape != k.shape or k.shape[1] != desc.num_kv_heads or k.shape[2] != desc.head_size:
+        raise ValueError("k/v must be [num_tokens][num_kv_heads][head_size] matching kv_cache")
+    if slot_mapping.shape[0] < t:
+        raise ValueError("slot_mapping is shorter than k")
+    _check(LIB.paged_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(kv_cache), ctypes.byref(desc),
+                              _ptr(status), _stream(stream)), "paged_kv_write")
+
+
+def paged_attention_workspace_bytes(max_num_reqs: int, max_num_tokens: int, num_q_heads: int, num_blocks: int,
+                                    num_kv_heads: int, head_size: int) -> int:
+    out = ctypes.c_size_t(0)
+    desc = CacheDesc(num_blocks, BLOCK_SIZE, num_kv_heads, head_size)
+    _check(LIB.paged_attention_workspace_bytes(max_num_reqs, max_num_tokens, num_q_heads, ctypes.byref(desc),
+                                               ctypes.byref(out)), "paged_attention_workspace_bytes")
+    return out.value
+
+
+def paged_attention_min_workspace_bytes(max_num_reqs: int, max_num_tokens: int, num_q_heads: int,
+                                        num_blocks: int, num_kv_heads: int, head_size: int) -> int:
+    out = ctypes.c_size_t(0)
+    desc = CacheDesc(num_blocks, BLOCK_SIZE, num_kv_heads, head_size)
+    _check(LIB.paged_attention_min_workspace_bytes(max_num_reqs, max_num_tokens, num_q_heads, ctypes.byref(desc),
+                                                   ctypes.byref(out)), "paged_attention_min_workspace_bytes")
+    return out.value
+
+
+def alloc_workspace(max_num_reqs: int, max_num_tokens: int, num_q_heads: int, kv_cache: torch.Tensor) -> torch.Tensor:
+    d = cache_desc(kv_cache)
+    nbytes = paged_attention_workspace_bytes(max_num_reqs, max_num_tokens, num_q_heads, d.num_blocks,
+                                             d.num_kv_heads, d.head_size)
+    # int64 elements: torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty((nbytes + 7) // 8, dtype=torch.int64, device=kv_cache.device)
+
+
+def paged_attention(q, kv_cache, block_table, seq_lens, query_start_loc, scale: float, out=None, workspace=None,
+                    stream=None, events=None) -> torch.Tensor:
+    """Attention over the paged pool. ``events``: optional four
+    torch.cuda.Event(enable_timing=True) recorded before the work-list
+    kernel, before and after the attention kernel, and after the merge."""
+    _want(q, torch.bfloat16, 3, "q")
+    _want(kv_cache, torch.bfloat16, 5, "kv_cache")
+    _want(block_table, torch.int32, 2, "block_table")
+    _want(seq_lens, torch.int32, 1, "seq_lens")
+    _want(query_start_loc, torch.int32, 1, "query_start_loc")
+    desc = cache_desc(kv_cache)
+    t, hq, d = q.shape
+    num_reqs = seq_lens.shape[0]
+    if d != desc.head_size:
+        raise ValueError("q head_size differs from kv_cache")
+    if query_start_loc.shape[0] != num_reqs + 1 or block_table.shape[0] != num_reqs:
+        raise ValueError("block_table, seq_lens and query_start_loc disagree on the number of requests")
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, torch.bfloat16, 3, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = alloc_workspace(num_reqs, t, hq, kv_cache)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    args = (_ptr(q), t, hq, _ptr(kv_cache), ctypes.byref(desc), _ptr(block_table), num_reqs, block_table.shape[1],
+            _ptr(seq_lens), _ptr(query_start_loc), float(scale), _ptr(out), _ptr(workspace), nbytes, _stream(stream))
+    if events is None:
+        _check(LIB.paged_attention(*args), "paged_attention")
+    else:
+        handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(_event_handle(e, stream)) for e in events])
+        _check(LIB.paged_attention_timed(*args, handles), "paged_attention_timed")
+    return out
+
+
+def _event_handle(ev, stream) -> int:
+    """Raw cudaEvent_t of a torch.cuda.Event (torch creates it on first record)."""
+    if ev is None:
+        return 0
+    if not ev.cuda_event:
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+    return int(ev.cuda_event)
+
+
+def pkv_read_status(status: torch.Tensor, stream=None) -> int:
+    """Device status word (synchronises the stream). For paged_attention pass
+    its workspace: the word is the workspace's first 4 bytes."""
+    v = ctypes.c_int32(0)
+    rc = LIB.pkv_read_status(_ptr(status), _stream(stream), ctypes.byref(v))
+    if rc not in (PKV_OK, PKV_E_DEVICE):
+        _check(rc, "pkv_read_status")
+    return v.value
+
+
+class StepBuffers:
+    """Device buffers of one paged-attention step for a fixed batch: the
+    metadata tables, slot mapping, output, workspace and status word."""
+
+    def __init__(self, batch, tensors: dict):
+        dev = tensors["q"].device
+        self.batch = batch
+        self.q = tensors["q"]
+        self.k = tensors["k"]
+        self.v = tensors["v"]
+        self.kv_cache = tensors["kv_cache"]
+        self.block_table = torch.from_numpy(batch.block_table).to(dev)
+        self.seq_lens = torch.from_numpy(batch.seq_lens).to(dev)
+        self.query_start_loc = torch.from_numpy(batch.query_start_loc).to(dev)
+        self.num_tokens = batch.num_tokens
+        self.slot_mapping = torch.empty(self.num_tokens, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.workspace = alloc_workspace(batch.num_reqs, self.num_tokens, batch.shape.num_q_heads, self.kv_cache)
+
+    def step(self, stream=None):
+        """Slot mapping, KV write and attention, enqueued on `stream`."""
+        paged_slot_mapping(self.block_table, self.seq_lens, self.query_start_loc, self.num_tokens,
+                           self.batch.num_blocks, self.slot_mapping, self.status, stream)
+        paged_kv_write(self.k, self.v, self.slot_mapping, self.kv_cache, self.status, stream)
+        paged_attention(self.q, self.kv_cache, self.block_table, self.seq_lens, self.query_start_loc,
+                        self.batch.scale, self.out, self.workspace, stream)
+        return self.out
+
+
+def run_step(batch, tensors: dict, stream=None) -> dict:
+    """One step on device tensors; raises if a device status bit is set."""
+    buf = StepBuffers(batch, tensors)
+    buf.step(stream)
+    st = pkv_read_status(buf.status, stream)
+    wst = pkv_read_status(buf.workspace, stream)
+    if st or wst:
+        raise PagedKVError(PKV_E_DEVICE, f"device status {st:#x} (slot/write) {wst:#x} (attention)")
+    return {"slot_mapping": buf.slot_mapping, "kv_cache": buf.kv_cache, "out": buf.out, "buffers": buf}

@@ -1,0 +1,132 @@
+// Slot mapping and KV write: the two bandwidth kernels in front of the
+// attention call ("Inside vLLM", page 1: "Run forward pass" step 2 builds
+// slot_mapping; the forward pass then populates the new tokens' KVs in paged
+// memory, "Prefix Caching").
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "pagedkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace {
+
+// Last r in [0, num_reqs) with qsl[r] <= t (qsl sorted ascending).
+__device__ __forceinline__ int find_request(const int32_t *__restrict__ qsl, int num_reqs, int t) {
+    int lo = 0, hi = num_reqs;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// One thread per new token.
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int num_reqs, int max_blocks_per_req,
+                                    const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ qsl,
+                                    int num_tokens, int num_blocks, int32_t *__restrict__ slot_mapping,
+                                    int32_t *status) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t == 0 && (__ldg(qsl) != 0 || __ldg(qsl + num_reqs) != num_tokens)) raise_status(status, PKV_DEV_BAD_QSL);
+    if (t >= num_tokens) return;
+    const int r = find_request(qsl, num_reqs, t);
+    const int q0 = __ldg(qsl + r), q1 = __ldg(qsl + r + 1);
+    int32_t slot = -1;
+    if (!(q0 <= t && t < q1)) {
+        raise_status(status, PKV_DEV_BAD_QSL);
+    } else {
+        const int n = q1 - q0;
+        const int L = __ldg(seq_lens + r);
+        const int pos = L - n + (t - q0);
+        if (n > L || (long long)L > (long long)max_blocks_per_req * PKV_BLOCK_SIZE || pos < 0) {
+            raise_status(status, PKV_DEV_BAD_LEN);
+        } else {
+            const int32_t blk = __ldg(block_table + (long long)r * max_blocks_per_req + pos / PKV_BLOCK_SIZE);
+            if (blk < 0 || blk >= num_blocks) raise_status(status, PKV_DEV_BAD_BLOCK);
+            else slot = blk * PKV_BLOCK_SIZE + pos % PKV_BLOCK_SIZE;
+        }
+    }
+    slot_mapping[t] = slot;
+}
+
+// One thread per 16-byte chunk of a (token, K|V, kv head) row; consecutive
+// threads walk a row, so reads of k/v and writes of each 16-row block tile
+// are contiguous.
+__global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                const int32_t *__restrict__ slot_mapping, long long num_tokens,
+                                uint4 *__restrict__ kv_cache, long long num_slots, int num_kv_heads,
+                                int chunks_per_row, int32_t *status) {
+    const long long per_kv = (long long)num_kv_heads * chunks_per_row;
+    const long long total = num_tokens * 2 * per_kv;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long t = idx / (2 * per_kv);
+        const long long rem = idx - t * 2 * per_kv;
+        const int kv = (int)(rem / per_kv);
+        const long long hc = rem - kv * per_kv;   // h * chunks_per_row + c
+        const int32_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if ((long long)slot >= num_slots) {
+            if (rem == 0) raise_status(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const int h = (int)(hc / chunks_per_row);
+        const int c = (int)(hc - (long long)h * chunks_per_row);
+        const uint4 val = __ldg((kv ? v : k) + t * per_kv + hc);
+        const long long block = slot / PKV_BLOCK_SIZE;
+        const int row = slot % PKV_BLOCK_SIZE;
+        const long long dst = (((block * 2 + kv) * num_kv_heads + h) * PKV_BLOCK_SIZE + row) * chunks_per_row + c;
+        kv_cache[dst] = val;
+    }
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" PKV_API int paged_slot_mapping(const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                                          const int32_t *seq_lens, const int32_t *query_start_loc,
+                                          int32_t num_tokens, int32_t num_blocks, int32_t *slot_mapping,
+                                          int32_t *status, void *stream) {
+    if (num_reqs < 0 || num_tokens < 0 || max_blocks_per_req < 0 || num_blocks <= 0) return PKV_E_DIMS;
+    if (num_blocks > INT32_MAX / PKV_BLOCK_SIZE) return PKV_E_DIMS;
+    if (num_tokens == 0) return PKV_OK;
+    if (num_reqs == 0) return PKV_E_DIMS;
+    if (!block_table || !seq_lens || !query_start_loc || !slot_mapping) return PKV_E_NULL;
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) ||
+        !aligned(slot_mapping, 4) || !aligned(status, 4))
+        return PKV_E_ALIGN;
+    const int threads = 256;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        block_table, num_reqs, max_blocks_per_req, seq_lens, query_start_loc, num_tokens, num_blocks, slot_mapping,
+        status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
+
+extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
+                                      void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream) {
+    if (!desc) return PKV_E_NULL;
+    int rc = check_cache_desc(*desc, /*attention=*/false);
+    if (rc) return rc;
+    if (num_tokens < 0) return PKV_E_DIMS;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !kv_cache) return PKV_E_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 4) ||
+        !aligned(status, 4))
+        return PKV_E_ALIGN;
+    const int chunks_per_row = desc->head_size / 8;
+    const long long total = (long long)num_tokens * 2 * desc->num_kv_heads * chunks_per_row;
+    const int threads = 256;
+    const long long want = (total + threads - 1) / threads;
+    const int blocks = (int)(want < (1 << 20) ? want : (1 << 20));
+    kv_write_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        static_cast<uint4 *>(kv_cache), (long long)desc->num_blocks * PKV_BLOCK_SIZE, desc->num_kv_heads,
+        chunks_per_row, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}

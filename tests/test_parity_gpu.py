@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Bars: slot mapping and KV write bit-exact (integer and byte work); attention
+within max-abs 2e-2 and mean-abs 2e-3 of the oracle (bf16 output).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_kv_gb300 import binding as pkv
+from paged_attention_kv_gb300 import workloads as wl
+
+from parity_utils import (assert_attention_close, device_tensors, host_inputs, oracle_step, run_gpu_step)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full(batch, ten, workspace_bytes=None, max_abs=2e-2, mean_abs=2e-3):
+    host = host_inputs(ten)
+    slots, pool, ref = oracle_step(batch, host)
+    buf, st, wst = run_gpu_step(batch, ten, workspace_bytes)
+    assert st == 0 and wst == 0, (hex(st), hex(wst))
+    assert np.array_equal(buf.slot_mapping.cpu().numpy(), slots)
+    assert np.array_equal(wl.bf16_bits(buf.kv_cache), pool)
+    assert_attention_close(buf.out, ref, max_abs=max_abs, mean_abs=mean_abs, what=batch.workload)
+    return buf, ref
+
+
+@pytest.mark.parametrize("workload", wl.WORKLOADS)
+def test_workload_parity_full(workload):
+    """All five workloads at full size: every slot, every pool byte, every
+    output element against the oracle."""
+    batch = wl.make_batch(workload)
+    ten = device_tensors(batch)
+    _check_full(batch, ten)
+
+
+def _custom(shape, seq, ql, seed, **kw):
+    return wl.custom_batch(shape, seq, ql, seed, **kw)
+
+
+LLAMA = wl.LLAMA3_8B
+TINY = wl.TINYLLAMA
+
+
+@pytest.mark.parametrize("shape", [TINY, LLAMA], ids=["d64", "d128"])
+def test_context_length_edges(shape):
+    seq = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000, 4097]
+    batch = _custom(shape, seq, [1] * len(seq), 101)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+@pytest.mark.parametrize("ql", [[4, 4, 4, 4], [2, 3, 5, 7], [17, 16, 15, 33]])
+def test_multi_token_queries(ql):
+    """Several new tokens per request (speculative verify, short chunks):
+    causal inside the chunk, tiles straddling token boundaries."""
+    seq = [40, 300, 17, 1200]
+    batch = _custom(LLAMA, seq, ql, 102)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+def test_prefill_chunks_and_fresh_prompts():
+    seq = [100, 700, 513, 64, 2000]
+    ql = [100, 200, 513, 1, 37]   # fresh prompts (n = L), a mid chunk, a decode
+    batch = _custom(LLAMA, seq, ql, 103)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 32, 128), (32, 16, 64), (32, 8, 64), (32, 4, 128), (32, 2, 128),
+                                      (32, 1, 64), (12, 4, 128), (20, 4, 64), (48, 8, 128)])
+def test_gqa_groups(hq, hkv, d):
+    shape = wl.ModelShape(f"h{hq}-{hkv}-{d}", hq, hkv, d)
+    seq = [33, 190, 1024, 7]
+    ql = [1, 3, 1, 7]
+    batch = _custom(shape, seq, ql, 104 + hq + hkv + d)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+def test_requests_without_new_tokens():
+    """A request with n = 0 contributes no rows and must not disturb others."""
+    seq = [50, 80, 20, 300, 1]
+    ql = [1, 0, 20, 0, 1]
+    batch = _custom(LLAMA, seq, ql, 105)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+def test_split_and_unsplit_agree():
+    """Minimal workspace (no room for split partials: one CTA per tile) and the
+    default (split-KV + merge) both match the oracle and each other."""
+    batch = _custom(LLAMA, [3000, 5000, 129, 777], [1, 2, 1, 1], 106)
+    ten = device_tensors(batch, generate_on="cpu")
+    pristine = {k: v.clone() for k, v in ten.items()}
+    s = batch.shape
+    minimal = pkv.paged_attention_min_workspace_bytes(batch.num_reqs, batch.num_tokens, s.num_q_heads,
+                                                      batch.num_blocks, s.num_kv_heads, s.head_size)
+    buf_a, ref = _check_full(batch, ten, workspace_bytes=minimal)
+    buf_b, _ = _check_full(batch, pristine)
+    assert float((buf_a.out.float() - buf_b.out.float()).abs().max()) <= 2e-2
+
+
+def test_block_permutation_is_bitwise_invariant():
+    """Relabelling physical blocks (and permuting the pool to match) gives the
+    same output bits: the arithmetic follows logical key order only."""
+    batch = _custom(LLAMA, [900, 47, 3000, 16], [1, 5, 1, 1], 107)
+    ten = device_tensors(batch, generate_on="cpu")
+    buf_a, _, _ = run_gpu_step(batch, {k: v.clone() for k, v in ten.items()})
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(batch.num_blocks).astype(np.int32)
+    batch2 = wl.Batch(**{**batch.__dict__})
+    bt = batch.block_table
+    batch2.block_table = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    pool2 = torch.empty_like(ten["kv_cache"])
+    pool2[torch.from_numpy(perm).long().to(pool2.device)] = ten["kv_cache"]
+    ten2 = {**{k: v.clone() for k, v in ten.items()}, "kv_cache": pool2}
+    buf_b, st, wst = run_gpu_step(batch2, ten2)
+    assert st == 0 and wst == 0
+    assert torch.equal(buf_a.out.view(torch.int16), buf_b.out.view(torch.int16))
+
+
+def test_chunked_prefill_equals_one_shot():
+    """A 2048-token prompt run as one chunk, and as four 512-token chunks
+    (each step writes its chunk's KV first): same pool bytes, outputs within
+    tolerance of each other and of the oracle."""
+    L = 2048
+    rng = np.random.default_rng(9)
+    g = torch.Generator().manual_seed(9)
+    shape = LLAMA
+    q = torch.randn(L, shape.num_q_heads, shape.head_size, generator=g).to(torch.bfloat16)
+    k = torch.randn(L, shape.num_kv_heads, shape.head_size, generator=g).to(torch.bfloat16)
+    v = torch.randn(L, shape.num_kv_heads, shape.head_size, generator=g).to(torch.bfloat16)
+    nb = 160
+    table = rng.permutation(nb)[:L // 16].astype(np.int32)[None, :]
+    pool0 = torch.randn(nb, 2, shape.num_kv_heads, 16, shape.head_size, generator=g).to(torch.bfloat16)
+
+    def batch_for(n, Lc):
+        return wl.Batch("chunk", shape, np.array([Lc], np.int32), np.array([n], np.int32), table, nb, 0)
+
+    dev = "cuda"
+    one = batch_for(L, L)
+    b1, st, wst = run_gpu_step(one, {"q": q.to(dev), "k": k.to(dev), "v": v.to(dev), "kv_cache": pool0.to(dev)})
+    assert st == 0 and wst == 0
+    pool = pool0.to(dev)
+    outs = []
+    for c in range(4):
+        lo, hi = c * 512, (c + 1) * 512
+        bc = batch_for(512, hi)
+        buf, st, wst = run_gpu_step(bc, {"q": q[lo:hi].to(dev), "k": k[lo:hi].to(dev), "v": v[lo:hi].to(dev),
+                                         "kv_cache": pool})
+        assert st == 0 and wst == 0
+        outs.append(buf.out)
+    chunked = torch.cat(outs)
+    assert torch.equal(b1.kv_cache.view(torch.int16), pool.view(torch.int16))
+    assert float((chunked.float() - b1.out.float()).abs().max()) <= 2e-2
+    host = {"q": wl.bf16_bits(q), "k": wl.bf16_bits(k), "v": wl.bf16_bits(v), "kv_cache": wl.bf16_bits(pool0)}
+    _, _, ref = oracle_step(one, host)
+    assert_attention_close(chunked, ref, what="chunked")
+    assert_attention_close(b1.out, ref, what="one-shot")
+
+
+def test_garbage_outside_context_is_never_used():
+    """Every pool slot outside the requests' contexts holds NaN; the outputs
+    must stay finite and match the oracle (masked keys contribute nothing)."""
+    batch = _custom(LLAMA, [17, 100, 1023, 45], [1, 3, 1, 45], 108)
+    ten = device_tensors(batch, generate_on="cpu")
+    full_qsl = np.concatenate([[0], np.cumsum(batch.seq_lens)]).astype(np.int32)
+    ctx = oracle.slot_mapping(batch.block_table, batch.seq_lens, full_qsl, batch.num_blocks)
+    pool = ten["kv_cache"].cpu()
+    keep = torch.zeros(batch.num_blocks * 16, dtype=torch.bool)
+    keep[torch.from_numpy(ctx).long()] = True
+    keep = keep.view(batch.num_blocks, 1, 1, 16, 1).expand_as(pool)
+    poisoned = torch.where(keep, pool, torch.full_like(pool, float("nan")))
+    ten["kv_cache"] = poisoned.to("cuda")
+    _check_full(batch, ten)
+
+
+def test_peaked_queries():
+    """Q scaled by 4: sharper softmax, a stricter check of the max handling."""
+    batch = _custom(LLAMA, [513, 2000, 64, 3333], [1, 1, 4, 1], 109)
+    ten = device_tensors(batch, generate_on="cpu")
+    ten["q"] = (ten["q"].float() * 4).to(torch.bfloat16)
+    _check_full(batch, ten)
+
+
+def test_bad_metadata_raises_status_without_fault():
+    """Out-of-range block ids, slots and lengths are skipped by the kernels'
+    own bounds checks and reported in the status words."""
+    batch = _custom(LLAMA, [40, 70], [1, 1], 110)
+    ten = device_tensors(batch, generate_on="cpu")
+    bad = wl.Batch(**{**batch.__dict__})
+    bad.block_table = batch.block_table.copy()
+    bad.block_table[1, 1] = batch.num_blocks + 7          # read by attention only
+    buf, st, wst = run_gpu_step(bad, {k: v.clone() for k, v in ten.items()})
+    assert wst & pkv.PKV_DEV_BAD_BLOCK
+    # KV write with a slot past the pool: skipped, pool untouched.
+    pool = ten["kv_cache"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([batch.num_blocks * 16 + 3, -1], dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write(ten["k"], ten["v"], slots, pool, status)
+    assert pkv.pkv_read_status(status) & pkv.PKV_DEV_BAD_SLOT
+    assert torch.equal(pool.view(torch.int16), ten["kv_cache"].view(torch.int16))
+    # More new tokens than context.
+    worse = wl.Batch(**{**batch.__dict__})
+    worse.seq_lens = np.array([40, 1], np.int32)
+    worse.query_lens = np.array([1, 2], np.int32)
+    ten3 = device_tensors(worse, generate_on="cpu")
+    buf, st, wst = run_gpu_step(worse, ten3)
+    assert st & pkv.PKV_DEV_BAD_LEN and wst & pkv.PKV_DEV_BAD_LEN
+
+
+def test_empty_batch_is_a_no_op():
+    q = torch.empty(0, 32, 128, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(4, 2, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(1, 1, dtype=torch.int32, device="cuda")
+    sl = torch.ones(1, dtype=torch.int32, device="cuda")
+    qsl = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = pkv.paged_attention(q, pool, bt, sl, qsl, 0.1)
+    assert out.numel() == 0
