@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV attention step on GB300.
+
+A step is the whole hot path over one batch: slot mapping, the KV write of
+the step's new tokens, and attention (work-list kernel, split-KV attention
+kernel, merge of split partials), all through the C ABI. The default
+workload is the Llama-3-8B-shaped decode batch (32 q / 8 kv heads, head 128,
+256 requests with contexts uniform in [512, 4096], block size 16); its pool
+(~3 GB) and per-step KV reads (~2.3 GB) are far larger than the 129 MB L2.
+
+Prints one JSON line. ``value`` is query tokens per second for the whole job
+(all ranks) with inputs resident in HBM; ``e2e`` is the same metric with
+each step's inputs copied from pinned host memory and the output copied back
+inside the timed region. ``roofline`` covers the attention kernel, timed
+live with CUDA events on its stream; ``cpu_baseline`` is the fp64 oracle on
+the host cores over a bounded sample of the same workload.
+
+``--impl reference`` times the oracle itself (the reference arm of this
+comparison) on the same workload and prints the same line shape.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+if REPO not in sys.path:
+    sys.path.insert(0, REPO)
+
+METRIC = "decode attention tokens/s and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "tokens/s"
+KERNEL_SOURCES = ("attention.cu", "attention_plan.cuh", "pkv_device.cuh")
+PROFILE_DOC = os.path.join(REPO, "profiles", "attention_decode_kernel_llama8b.md")
+LAUNCHES_PER_STEP = 5  # slot mapping, KV write, work list, attention, merge
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="llama8b")
+    p.add_argument("--skip-cpu-baseline", action="store_true", help="leave out the oracle CPU baseline")
+    p.add_argument("--skip-e2e", action="store_true", help="leave out the end-to-end (host buffers) loop")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# workload bookkeeping (measurement only)
+# --------------------------------------------------------------------------
+
+def workload_config(batch) -> dict:
+    s = batch.shape
+    return {
+        "workload": batch.workload,
+        "description": batch.description,
+        "shape": f"{s.name} attention ({s.num_q_heads} q / {s.num_kv_heads} kv heads, head {s.head_size})",
+        "num_reqs": batch.num_reqs,
+        "num_tokens": batch.num_tokens,
+        "block_size": 16,
+        "num_blocks": batch.num_blocks,
+        "context_tokens": int(batch.seq_lens.sum()),
+        "l2": "inputs larger than L2 (per-step KV reads of GBs vs 129 MB L2), no flush",
+    }
+
+
+def algorithmic_bytes(batch) -> dict:
+    """Bytes one attention launch must move at minimum: every context
+    token's K and V once (blocks shared by several requests counted once),
+    Q read, output written, the block-table entries used and the per-request
+    metadata."""
+    s = batch.shape
+    rows_used = {}
+    for r, L in enumerate(batch.seq_lens):
+        L = int(L)
+        nb = -(-L // 16)
+        for j in range(nb):
+            b = int(batch.block_table[r, j])
+            rows = min(16, L - 16 * j)
+            if rows_used.get(b, 0) < rows:
+                rows_used[b] = rows
+    unique_tokens = sum(rows_used.values())
+    per_token = 2 * s.num_kv_heads * s.head_size * 2
+    kv = unique_tokens * per_token
+    logical_kv = int(batch.seq_lens.sum()) * per_token
+    qo = 2 * batch.num_tokens * s.num_q_heads * s.head_size * 2
+    bt = int(sum(-(-int(L) // 16) for L in batch.seq_lens)) * 4
+    meta = (2 * batch.num_reqs + 1) * 4
+    return {"kv": kv, "logical_kv": logical_kv, "q_out": qo, "block_table": bt, "meta": meta,
+            "attention_total": kv + qo + bt + meta, "unique_tokens": unique_tokens}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(REPO, "paged_attention_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    try:
+        text = open(PROFILE_DOC).read()
+    except OSError:
+        return None
+    src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------
+# ranks (weak scaling: independent batches, no data-path collective)
+# --------------------------------------------------------------------------
+
+def rank_batch(workload: str, rank: int):
+    """Rank r runs its own batch of the workload's shape, drawn from a seed
+    offset by 1000 r."""
+    from paged_attention_kv_gb300 import workloads as wl
+    return wl.make_batch(workload, seed_offset=1000 * rank)
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The slowest rank's time (the job's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Query tokens all ranks processed per second of the slowest rank."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-i",
+                 str(gpu_index), "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed"
+        if len(inside) < 3:
+            inside, window = rows, "warmup+timed"
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------
+# oracle (CPU baseline and reference arm)
+# --------------------------------------------------------------------------
+
+def sub_batch(batch, reqs):
+    from paged_attention_kv_gb300 import workloads as wl
+    reqs = np.asarray(reqs)
+    return wl.Batch(workload=batch.workload, shape=batch.shape, seq_lens=batch.seq_lens[reqs],
+                    query_lens=batch.query_lens[reqs], block_table=batch.block_table[reqs],
+                    num_blocks=batch.num_blocks, seed=batch.seed)
+
+
+def oracle_step(batch, host, reqs, threads):
+    """Slot mapping, KV write and attention of the requests `reqs` on the
+    host cores; returns the query tokens processed."""
+    import oracle
+    sb = sub_batch(batch, reqs)
+    qsl_full = batch.query_start_loc
+    tok = np.concatenate([np.arange(qsl_full[r], qsl_full[r + 1]) for r in reqs])
+    slots = oracle.slot_mapping(sb.block_table, sb.seq_lens, sb.query_start_loc, sb.num_blocks)
+    oracle.kv_write(host["kv_cache"], host["k"][tok], host["v"][tok], slots)
+    oracle.paged_attention(host["q"][tok], host["kv_cache"], sb.block_table, sb.seq_lens, sb.query_start_loc,
+                           sb.scale, num_threads=threads)
+    return int(sb.num_tokens)
+
+
+def host_copy(ten):
+    from paged_attention_kv_gb300 import workloads as wl
+    return {k: wl.bf16_bits(v).copy() for k, v in ten.items()}
+
+
+def cpu_baseline(batch, host, target_s=10.0, cap_s=30.0) -> dict:
+    """The oracle as it stands on every host core, over whole requests of
+    the workload, repeated until about target_s of work."""
+    threads = os.cpu_count() or 1
+    order = np.arange(batch.num_reqs)
+    t0 = time.perf_counter()
+    tokens = oracle_step(batch, host, order[:4], threads)
+    per_req = (time.perf_counter() - t0) / 4
+    n = int(min(batch.num_reqs, max(4, target_s / max(per_req, 1e-6))))
+    done, reqs_done, start = 0, 0, time.perf_counter()
+    i = 0
+    while time.perf_counter() - start < target_s and time.perf_counter() - start < cap_s:
+        sel = order[(np.arange(n) + i) % batch.num_reqs]
+        done += oracle_step(batch, host, sel, threads)
+        reqs_done += n
+        i += n
+    el = time.perf_counter() - start
+    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{reqs_done} requests of the {batch.workload} workload ({done} query tokens, whole "
+                      f"step: slot mapping + KV write + attention), fp64, {el:.1f} s"}
+
+
+def run_reference(args, batch, rank):
+    """The reference arm: the oracle timed on the host cores."""
+    from paged_attention_kv_gb300 import workloads as wl
+    if rank != 0:
+        return
+    ten = wl.make_tensors(batch, device="cpu")
+    host = host_copy(ten)
+    threads = os.cpu_count() or 1
+    # size each step's sample so warmup + steps stay within ~2 minutes
+    t0 = time.perf_counter()
+    oracle_step(batch, host, np.arange(2), threads)
+    per_req = (time.perf_counter() - t0) / 2
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(min(batch.num_reqs, max(1, budget / max(per_req, 1e-6))))
+    reqs = [np.arange(i * n, (i + 1) * n) % batch.num_reqs for i in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        oracle_step(batch, host, reqs[i], threads)
+    start = time.perf_counter()
+    tokens = 0
+    for i in range(args.steps):
+        tokens += oracle_step(batch, host, reqs[args.warmup + i], threads)
+    el = time.perf_counter() - start
+    value = tokens / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(batch),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} requests of {batch.workload} per step (whole step, fp64)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    batch = rank_batch(args.workload, rank)
+
+    if args.impl == "reference":
+        run_reference(args, batch, rank)
+        return
+
+    import torch
+    from paged_attention_kv_gb300 import binding as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    ten = wl.make_tensors(batch, device=dev)
+    host = host_copy(ten) if (rank == 0 and world == 1 and not args.skip_cpu_baseline) else None
+    buf = pkv.StepBuffers(batch, ten)
+    stream = torch.cuda.current_stream()
+
+    nev = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nev)]
+
+    def step(i=None):
+        pkv.paged_slot_mapping(buf.block_table, buf.seq_lens, buf.query_start_loc, buf.num_tokens,
+                               batch.num_blocks, buf.slot_mapping, buf.status)
+        pkv.paged_kv_write(buf.k, buf.v, buf.slot_mapping, buf.kv_cache, buf.status)
+        pkv.paged_attention(buf.q, buf.kv_cache, buf.block_table, buf.seq_lens, buf.query_start_loc, batch.scale,
+                            buf.out, buf.workspace, events=None if i is None else ev[i])
+
+    sampler = ClockSampler(local_rank)
+    for _ in range(args.warmup):
+        step()
+    # create the event handles outside the timed region
+    for e4 in ev:
+        for e in e4:
+            e.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist:
+        dist.barrier()
+    sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    st = pkv.pkv_read_status(buf.status)
+    wst = pkv.pkv_read_status(buf.workspace)
+    if st or wst:
+        raise RuntimeError(f"device status bits set: {st:#x} {wst:#x}")
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+
+    attn_ms = [e4[1].elapsed_time(e4[2]) for e4 in ev]
+    attn_call_ms = [e4[0].elapsed_time(e4[3]) for e4 in ev]
+    kernel_ms = float(np.mean(attn_ms))
+
+    # end to end: inputs from pinned host memory, output back, every step
+    e2e = None
+    if not args.skip_e2e:
+        e2e = run_e2e(args, batch, ten, buf, pkv, torch, dev, dist)
+
+    cpu = None
+    if host is not None:
+        cpu = cpu_baseline(batch, host)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    ab = algorithmic_bytes(batch)
+    peaks = measured_peaks()
+    achieved = ab["attention_total"] / (kernel_ms * 1e-3) / 1e9
+    ms_per_step = elapsed_ms / args.steps
+    value = job_tokens_per_s(world, batch.num_tokens, ms_per_step)
+    clocks = sampler.summary(wall0, wall1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block tables)",
+        "config": {**workload_config(batch), "parallelism": f"{world} independent replicas" if world > 1
+                   else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "attention decode_kernel (split-KV)", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": ab["attention_total"],
+                     "kernel_us": kernel_ms * 1e3, "attention_call_us": float(np.mean(attn_call_ms)) * 1e3,
+                     "frac_of_8tbps_nominal": achieved / 8000.0},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "kv_bytes_per_step": {"unique": ab["kv"], "logical": ab["logical_kv"]},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, batch, ten, buf, pkv, torch, dev, dist):
+    """K steps through the public API with this step's inputs (q, k, v and
+    the metadata tables) copied from pinned host memory and the output copied
+    back, all inside the timed region. The pool stays resident: it is the
+    layer's KV state, not a per-step input."""
+    host_in = {
+        "q": ten["q"].cpu().pin_memory(), "k": ten["k"].cpu().pin_memory(), "v": ten["v"].cpu().pin_memory(),
+        "block_table": buf.block_table.cpu().pin_memory(), "seq_lens": buf.seq_lens.cpu().pin_memory(),
+        "query_start_loc": buf.query_start_loc.cpu().pin_memory(),
+    }
+    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_host.numel() * out_host.element_size()
+    slots = torch.empty(batch.num_tokens, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        pkv.paged_slot_mapping(dev_in["block_table"], dev_in["seq_lens"], dev_in["query_start_loc"],
+                               batch.num_tokens, batch.num_blocks, slots, status)
+        pkv.paged_kv_write(dev_in["k"], dev_in["v"], slots, buf.kv_cache, status)
+        pkv.paged_attention(dev_in["q"], buf.kv_cache, dev_in["block_table"], dev_in["seq_lens"],
+                            dev_in["query_start_loc"], batch.scale, buf.out, buf.workspace)
+        out_host.copy_(buf.out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    ms = max_over_ranks(ms, dist, dev)
+    world = dist.get_world_size() if dist else 1
+    return {"value": job_tokens_per_s(world, batch.num_tokens, ms / args.steps), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+if __name__ == "__main__":
+    main()
