@@ -192,6 +192,38 @@ int paged_attention_timed(const void *q, int32_t num_tokens, int32_t num_q_heads
                           void *const *events);
 
 /*
+ * paged_attention without a workspace argument, for callers that cannot
+ * allocate device memory at the point where they run attention: an engine
+ * that has already given nearly all free device memory to its KV pool (the
+ * pages size the pool to fill what a profiling pass leaves), a plugin whose
+ * host framework owns all device memory, or a latency-critical loop that
+ * cannot take cudaMalloc's implicit synchronisation. The paper has no
+ * counterpart to this entry point; it exists for those callers.
+ *
+ * The work list and split-KV partials live in one fixed 16 MiB device
+ * array inside this library, which every GPU that loads the library keeps
+ * until the process exits; the call allocates nothing. A batch whose work
+ * list does not fit in 16 MiB (about 150k new tokens at 32 query heads) is
+ * rejected with PKV_E_WORKSPACE; a large batch that fits gets fewer
+ * split-KV partitions than paged_attention would give it.
+ *
+ * The first call on each device looks up the array's device address and
+ * sets up the kernels (with that device current); make that first call
+ * before any stream capture. All calls on a device share the one array and
+ * it keeps the previous call's contents (each call rebuilds what it reads),
+ * so calls whose work overlaps on the GPU race with each other: issue them
+ * on one stream, or order them. The device status word of this variant
+ * stays inside the array and cannot be read back; bad metadata is still
+ * skipped safely. Arguments, layouts and results are otherwise those of
+ * paged_attention.
+ */
+int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                           const void *kv_cache, const pkv_cache_desc *desc,
+                           const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                           const int32_t *seq_lens, const int32_t *query_start_loc,
+                           float scale, void *out, void *stream);
+
+/*
  * Copies a device status word to *host_status after the work queued on
  * `stream` so far has finished (synchronises the stream). Returns PKV_OK if
  * the word is 0, PKV_E_DEVICE if bits are set, PKV_E_CUDA on a CUDA error.

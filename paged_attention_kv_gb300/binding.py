@@ -38,8 +38,8 @@ PKV_DEV_TIMEOUT = 0x10
 PKV_DEV_OVERFLOW = 0x20
 
 EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_attention_workspace_bytes",
-            "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed", "pkv_read_status",
-            "pkv_status_string")
+            "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
+            "paged_attention_static", "pkv_read_status", "pkv_status_string")
 
 
 class PagedKVError(RuntimeError):
@@ -66,6 +66,7 @@ def _load():
     lib.paged_attention_min_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
     lib.paged_attention.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.paged_attention_timed.argtypes = lib.paged_attention.argtypes + [ctypes.POINTER(vp)]
+    lib.paged_attention_static.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp]
     lib.pkv_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -218,6 +219,28 @@ def paged_attention(q, kv_cache, block_table, seq_lens, query_start_loc, scale: 
     else:
         handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(_event_handle(e, stream)) for e in events])
         _check(LIB.paged_attention_timed(*args, handles), "paged_attention_timed")
+    return out
+
+
+def paged_attention_static(q, kv_cache, block_table, seq_lens, query_start_loc, scale: float, out,
+                           stream=None) -> torch.Tensor:
+    """paged_attention without a workspace: for callers that cannot allocate
+    device memory when they run attention (the library's fixed 16 MiB scratch
+    array is used instead). ``out`` must be preallocated. Calls on one
+    device share that array, so they must not overlap on the GPU."""
+    _want(q, torch.bfloat16, 3, "q")
+    _want(kv_cache, torch.bfloat16, 5, "kv_cache")
+    _want(block_table, torch.int32, 2, "block_table")
+    _want(seq_lens, torch.int32, 1, "seq_lens")
+    _want(query_start_loc, torch.int32, 1, "query_start_loc")
+    _want(out, torch.bfloat16, 3, "out")
+    desc = cache_desc(kv_cache)
+    t, hq, _ = q.shape
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(LIB.paged_attention_static(_ptr(q), t, hq, _ptr(kv_cache), ctypes.byref(desc), _ptr(block_table),
+                                      seq_lens.shape[0], block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+                                      float(scale), _ptr(out), _stream(stream)), "paged_attention_static")
     return out
 
 

@@ -913,3 +913,56 @@ extern "C" PKV_API int paged_attention_timed(const void *q, int32_t num_tokens, 
     return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
                           seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, events);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant
+// ---------------------------------------------------------------------------
+// Some callers cannot allocate device memory when they call attention: an
+// engine that, after its profiling pass, has handed almost all free device
+// memory to the KV pool; a plugin whose host framework owns the device
+// memory and offers it no allocator; a latency-critical loop where
+// cudaMalloc's implicit synchronisation is not acceptable. For them the
+// work list and split partials live in this fixed array instead of a
+// caller-provided workspace. Every GPU that loads this library holds the
+// array until the process exits.
+
+static constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace pkv {
+namespace {
+
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64] = {};
+
+// Device address of g_static_scratch on the current device. In host code the
+// symbol itself is only a host-side stand-in, so the address is looked up
+// once per device with that device current.
+int static_scratch_address(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_E_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PKV_E_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" PKV_API int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                                              const void *kv_cache, const pkv_cache_desc *desc,
+                                              const int32_t *block_table, int32_t num_reqs,
+                                              int32_t max_blocks_per_req, const int32_t *seq_lens,
+                                              const int32_t *query_start_loc, float scale, void *out, void *stream) {
+    if (!desc) return PKV_E_NULL;
+    void *scratch = nullptr;
+    const int rc = static_scratch_address(&scratch);
+    if (rc) return rc;
+    return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
+                          seq_lens, query_start_loc, scale, out, scratch, kStaticScratchBytes, stream, nullptr);
+}
