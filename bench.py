@@ -2,8 +2,8 @@
 """Benchmark of one paged-KV attention step on GB300.
 
 A step is the whole hot path over one batch: slot mapping, the KV write of
-the step's new tokens, and attention (work-list kernel, split-KV attention
-kernel, merge of split partials), all through the C ABI. The default
+the step's new tokens, and attention (work-list kernel, then the split-KV
+attention kernel, which also merges split partials), all through the C ABI. The default
 workload is the Llama-3-8B-shaped decode batch (32 q / 8 kv heads, head 128,
 256 requests with contexts uniform in [512, 4096], block size 16); its pool
 (~3 GB) and per-step KV reads (~2.3 GB) are far larger than the 129 MB L2.
@@ -39,7 +39,7 @@ METRIC = "decode attention tokens/s and achieved HBM GB/s (fraction of GB300 pea
 UNIT = "tokens/s"
 KERNEL_SOURCES = ("attention.cu", "attention_plan.cuh", "pkv_device.cuh")
 PROFILE_DOC = os.path.join(REPO, "profiles", "attention_decode_kernel_llama8b.md")
-LAUNCHES_PER_STEP = 5  # slot mapping, KV write, work list, attention, merge
+LAUNCHES_PER_STEP = 4  # slot mapping, KV write, work list, attention (split merge folded in)
 
 
 def parse_args():
@@ -317,6 +317,7 @@ def main():
 
     import torch
     from paged_attention_kv_gb300 import binding as pkv
+    from paged_attention_kv_gb300 import workloads as wl
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)

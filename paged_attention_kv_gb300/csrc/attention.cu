@@ -2,17 +2,20 @@
 // forward pass" step 3: one super sequence, each sequence attending only to
 // its own tokens; decode and chunked-prefill requests mixed in one step).
 //
-// Three launches on the caller's stream:
+// Two launches on the caller's stream:
 //   plan_kernel    one CTA turns query_start_loc / seq_lens into a work list
-//                  (attention_plan.cuh), choosing the split-KV length so the
-//                  persistent grid gets ~kItemsPerCta items per CTA;
-//   decode_kernel  persistent, warp-specialised: one producer warp gathers
-//                  each K/V block tile (16 rows x D, contiguous in the pool)
-//                  with TMA into a shared-memory ring; four consumer warps run
-//                  S = Q K^T and O += P V on bf16 mma.sync tensor-core tiles
-//                  with an fp32 online softmax (exp2 domain), then combine
-//                  their partial states in shared memory;
-//   merge_kernel   combines the split partials of tiles with several splits.
+//                  (attention_plan.cuh): it picks the split-KV length so the
+//                  persistent grid gets ~kItemsPerCta items per CTA and lists
+//                  the items longest first;
+//   decode_kernel  persistent, warp-specialised. One producer warp takes
+//                  items from an atomic counter, bulk-copies each item's Q
+//                  rows and gathers each K/V block tile (16 rows x D,
+//                  contiguous in the pool) with TMA into a shared-memory
+//                  ring; four consumer warps run S = Q K^T and O += P V on
+//                  bf16 mma.sync tensor-core tiles with an fp32 online
+//                  softmax (exp2 domain), combine their states in shared
+//                  memory, and either write the output or a split partial;
+//                  the CTA finishing a tile's last split merges its partials.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -43,11 +46,13 @@ struct PlanArgs {
     const int32_t *qsl;
     const int32_t *seq_lens;
     int num_reqs, num_tokens, max_blocks_per_req, group, num_kv_heads;
-    long long target_items, parts_cap, groups_cap, items_cap;
+    int block_bytes_kv;  // K + V bytes of one (block, kv head): 2 * 16 * D * 2
+    long long target_items, part_rows_cap, groups_cap, items_cap;
     WsHeader *header;
-    int32_t *req_group_base;
+    int32_t *req_cache;  // 4 * (num_reqs + 1) ints, used when the batch has too many requests for shared memory
+    int32_t *group_req;
     int32_t *group_kvb;
-    int2 *tile_info;
+    int32_t *tile_counter;
     WorkItem *items;
 };
 
@@ -94,46 +99,75 @@ __device__ __forceinline__ int tile_kv_end(int n, int L, int g, int mt) {
     return L - n + (int)(last_row / g) + 1;
 }
 
-__device__ __forceinline__ int find_group_request(const int32_t *req_group_base, int num_reqs, int gi) {
-    int lo = 0, hi = num_reqs;  // last r with base[r] <= gi, requests with no tiles skipped
+__device__ __forceinline__ int tile_rows(int n, int g, int mt) {
+    return (int)min((long long)kRowsPerTile, (long long)n * g - (long long)mt * kRowsPerTile);
+}
+
+// Last r in [0, num_reqs) with base[r] <= gi (requests without tiles are skipped).
+__device__ __forceinline__ int find_group_request(const int32_t *base, int num_reqs, int gi) {
+    int lo = 0, hi = num_reqs;
     while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (req_group_base[mid] <= gi) lo = mid; else hi = mid;
+        const int mid = (lo + hi) >> 1;
+        if (base[mid] <= gi) lo = mid; else hi = mid;
     }
     return lo;
 }
 
+// Size bucket of an item of `size` blocks: 0 for a full split, then 1..8
+// from longest to shortest.
+__device__ __forceinline__ int size_bucket(int size, int split) {
+    if (size >= split) return 0;
+    return kSizeBuckets - 1 - min(kSizeBuckets - 2, (int)((long long)size * (kSizeBuckets - 1) / split));
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
+    extern __shared__ int32_t s_req[];  // 4 * (kPlanSmemReqs + 1) ints when the batch fits
     __shared__ long long s_ll[32];
     __shared__ int s_i[32];
     __shared__ int s_split;
+    __shared__ int s_bucket_count[kSizeBuckets], s_bucket_base[kSizeBuckets], s_bucket_cursor[kSizeBuckets];
     const int tid = threadIdx.x;
+    const int R = a.num_reqs, Hkv = a.num_kv_heads, g = a.group;
     int32_t *status = &a.header->status;
+    const int stride = R + 1;
+    int32_t *cache = R <= kPlanSmemReqs ? s_req : a.req_cache;
+    int32_t *req_n = cache, *req_L = cache + stride, *req_q0 = cache + 2 * stride, *req_g = cache + 3 * stride;
+
     if (tid == 0) {
         a.header->status = 0;
-        if (a.qsl[0] != 0 || a.qsl[a.num_reqs] != a.num_tokens) atomicOr(status, PKV_DEV_BAD_QSL);
+        a.header->next_item = 0;
+        if (a.qsl[0] != 0 || a.qsl[R] != a.num_tokens) atomicOr(status, PKV_DEV_BAD_QSL);
+    }
+    if (tid < kSizeBuckets) {
+        s_bucket_count[tid] = 0;
+        s_bucket_cursor[tid] = 0;
     }
     __syncthreads();
 
-    // 1. tiles per request -> req_group_base (exclusive scan, chunked).
+    // 1. validate requests, cache (n, L, q0), tiles per request -> group base.
     int carry = 0;
-    for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
+    for (int base = 0; base < R; base += kPlanThreads) {
         const int r = base + tid;
         int mtiles = 0;
-        if (r < a.num_reqs) {
+        if (r < R) {
             const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
             const int n = q1 - q0;
+            bool ok = false;
             if (n < 0 || q0 < 0 || q1 > a.num_tokens) {
                 atomicOr(status, PKV_DEV_BAD_QSL);
             } else if (n > L || (long long)L > (long long)a.max_blocks_per_req * PKV_BLOCK_SIZE) {
                 atomicOr(status, PKV_DEV_BAD_LEN);
             } else {
-                mtiles = (int)(((long long)n * a.group + kRowsPerTile - 1) / kRowsPerTile);
+                ok = true;
+                mtiles = (int)(((long long)n * g + kRowsPerTile - 1) / kRowsPerTile);
             }
+            req_n[r] = ok ? n : 0;
+            req_L[r] = L;
+            req_q0[r] = q0;
         }
         int chunk_total;
         const int ex = block_exclusive_scan<int>(mtiles, &chunk_total, s_i);
-        if (r < a.num_reqs) a.req_group_base[r] = carry + ex;
+        if (r < R) req_g[r] = carry + ex;
         carry += chunk_total;
     }
     int n_groups = carry;
@@ -143,95 +177,117 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         if (tid == 0) atomicOr(status, PKV_DEV_OVERFLOW);
         n_groups = (int)a.groups_cap;
         __syncthreads();
-        for (int r = tid; r < a.num_reqs; r += kPlanThreads)
-            a.req_group_base[r] = min(a.req_group_base[r], n_groups);
+        for (int r = tid; r < R; r += kPlanThreads) req_g[r] = min(req_g[r], n_groups);
     }
-    if (tid == 0) a.req_group_base[a.num_reqs] = n_groups;
+    if (tid == 0) req_g[R] = n_groups;
     __syncthreads();
 
     // 2. keys per group, total work in block loads.
     long long work = 0;
     for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
-        const int r = find_group_request(a.req_group_base, a.num_reqs, gi);
-        const int mt = gi - a.req_group_base[r];
-        const int n = a.qsl[r + 1] - a.qsl[r], L = a.seq_lens[r];
-        const int kvb = (tile_kv_end(n, L, a.group, mt) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+        const int r = find_group_request(req_g, R, gi);
+        const int mt = gi - req_g[r];
+        const int kvb = (tile_kv_end(req_n[r], req_L[r], g, mt) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+        a.group_req[gi] = r;
         a.group_kvb[gi] = kvb;
-        work += (long long)kvb * a.num_kv_heads;
+        work += (long long)kvb * Hkv;
     }
-    work = block_sum<long long>(work, s_ll);
+    work = block_sum<long long>(work, s_ll);  // (its barriers also publish group_req / group_kvb)
 
-    // 3. split length: about target_items items, partials within capacity.
+    // 3. split length: about target_items items, partial rows within capacity.
     if (tid == 0) {
         long long s = (work + a.target_items - 1) / max(1LL, a.target_items);
         s = max(s, (long long)kMinSplitBlocks);
-        if (a.parts_cap <= 0) s = INT_MAX / 2;
+        s = max(s, (long long)(kMinItemBytes / a.block_bytes_kv));
+        if (a.part_rows_cap <= 0) s = INT_MAX / 2;
         s_split = (int)min(s, (long long)(INT_MAX / 2));
     }
     __syncthreads();
     while (true) {
         const int split = s_split;
-        long long parts = 0;
+        long long rows = 0;
         for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
             const int ns = (a.group_kvb[gi] + split - 1) / split;
-            if (ns > 1) parts += (long long)ns * a.num_kv_heads;
+            if (ns > 1) {
+                const int r = a.group_req[gi];
+                rows += (long long)ns * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
+            }
         }
-        parts = block_sum<long long>(parts, s_ll);
-        if (parts <= a.parts_cap) break;
-        if (tid == 0) s_split = split * 2;
+        rows = block_sum<long long>(rows, s_ll);
+        if (rows <= a.part_rows_cap) break;
+        if (tid == 0) s_split = split > INT_MAX / 4 ? INT_MAX / 2 : split * 2;
         __syncthreads();
     }
     const int split = s_split;
 
-    // 4. items and tile info, chunked scans over groups.
-    int item_carry = 0, part_carry = 0;
+    // 4. count items per size bucket.
+    for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
+        const int kvb = a.group_kvb[gi];
+        const int ns = max(1, (kvb + split - 1) / split);
+        const int last = kvb - (ns - 1) * split;
+        if (ns > 1) atomicAdd(&s_bucket_count[0], (ns - 1) * Hkv);
+        atomicAdd(&s_bucket_count[size_bucket(last, split)], Hkv);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int b = 0; b < kSizeBuckets; ++b) {
+            s_bucket_base[b] = acc;
+            acc += s_bucket_count[b];
+        }
+        a.header->n_items = (int)min((long long)acc, a.items_cap);
+        if (acc > a.items_cap) atomicOr(status, PKV_DEV_OVERFLOW);
+    }
+    __syncthreads();
+
+    // 5. partial-row bases (chunked scan over groups) and the items.
+    int row_carry = 0;
     for (int base = 0; base < n_groups; base += kPlanThreads) {
         const int gi = base + tid;
-        int ns = 0, r = 0, mt = 0, kvb = 0;
+        int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
         if (gi < n_groups) {
-            r = find_group_request(a.req_group_base, a.num_reqs, gi);
-            mt = gi - a.req_group_base[r];
+            r = a.group_req[gi];
+            mt = gi - req_g[r];
             kvb = a.group_kvb[gi];
             ns = max(1, (kvb + split - 1) / split);
+            nv = tile_rows(req_n[r], g, mt);
         }
-        const int n_it = gi < n_groups ? ns * a.num_kv_heads : 0;
-        const int n_pt = (gi < n_groups && ns > 1) ? ns * a.num_kv_heads : 0;
-        int tot_it, tot_pt;
-        const int it0 = item_carry + block_exclusive_scan<int>(n_it, &tot_it, s_i);
-        const int pt0 = part_carry + block_exclusive_scan<int>(n_pt, &tot_pt, s_i);
+        const int n_rows = (gi < n_groups && ns > 1) ? ns * Hkv * nv : 0;
+        int tot_rows;
+        const int row0 = row_carry + block_exclusive_scan<int>(n_rows, &tot_rows, s_i);
         if (gi < n_groups) {
-            const int q0 = a.qsl[r], n = a.qsl[r + 1] - q0, L = a.seq_lens[r];
-            const int kv_end = tile_kv_end(n, L, a.group, mt);
-            for (int h = 0; h < a.num_kv_heads; ++h) {
-                const long long tile = (long long)gi * a.num_kv_heads + h;
-                const int pbase = ns > 1 ? pt0 + h * ns : -1;
-                a.tile_info[tile] = make_int2(ns, pbase);
+            const int n = req_n[r], L = req_L[r], q0 = req_q0[r];
+            const int kv_end = tile_kv_end(n, L, g, mt);
+            for (int h = 0; h < Hkv; ++h) {
+                const int tile = gi * Hkv + h;
+                const int prow0 = ns > 1 ? row0 + h * ns * nv : -1;
+                if (ns > 1) a.tile_counter[tile] = 0;
                 for (int s = 0; s < ns; ++s) {
-                    const long long idx = (long long)it0 + (long long)h * ns + s;
-                    if (idx >= a.items_cap) { atomicOr(status, PKV_DEV_OVERFLOW); continue; }
                     const int kb0 = s * split;
                     const int kb1 = min(kvb, kb0 + split);
+                    const int b = size_bucket(kb1 - kb0, split);
+                    const long long idx = (long long)s_bucket_base[b] + atomicAdd(&s_bucket_cursor[b], 1);
+                    if (idx >= a.items_cap) continue;
                     WorkItem w;
                     w.a = make_int4(r, mt, h, s);
-                    w.b = make_int4(kb0, kb1, ns > 1 ? pbase + s : -1, q0);
-                    w.c = make_int4(n, L, kv_end, 0);
+                    w.b = make_int4(kb0, kb1, prow0, q0);
+                    w.c = make_int4(n, L, kv_end, tile);
+                    w.d = make_int4(ns, nv, 0, 0);
                     a.items[idx] = w;
                 }
             }
         }
-        item_carry += tot_it;
-        part_carry += tot_pt;
+        row_carry += tot_rows;
     }
     if (tid == 0) {
-        a.header->n_items = (int)min((long long)item_carry, a.items_cap);
         a.header->split_blocks = split;
         a.header->n_groups = n_groups;
-        a.header->n_partials = part_carry;
+        a.header->n_partial_rows = row_carry;
     }
 }
 
 // ---------------------------------------------------------------------------
-// decode (split-KV) kernel
+// split-KV attention kernel
 // ---------------------------------------------------------------------------
 
 struct DecodeArgs {
@@ -242,14 +298,15 @@ struct DecodeArgs {
     float scale_log2;
     const WorkItem *items;
     WsHeader *header;
+    int32_t *tile_counter;
     float2 *part_ml;
     float *part_o;
 };
 
 // Per-item description handed from the producer to the consumers through
-// shared memory, next to the item's Q rows.
+// shared memory, next to the item's Q rows. item < 0 ends the CTA's loop.
 struct ItemDesc {
-    int kb0, kb1, part, n_valid, kv_end, h, pad0, pad1;
+    int item, kb0, kb1, part_row0, n_valid, kv_end, s, ns, tile, pad[7];
     int row_t[kRowsPerTile];
     int row_hq[kRowsPerTile];
     int row_limit[kRowsPerTile];
@@ -261,7 +318,7 @@ struct DecodeSmem {
     static constexpr int kTileBytes = kBoxes * 2048;        // 16 rows x D bf16
     static constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
     static constexpr int kStages = D == 128 ? 8 : 12;
-    static constexpr int kQStride = 2 * D + 16;             // padded row: conflict-free ldmatrix
+    static constexpr int kQStride = 2 * D;                  // Q rows as bulk-copied from q
     static constexpr int kQBytes = kRowsPerTile * kQStride;
     static constexpr int kScrStride = D + 8;                // floats per scratch row
     static constexpr int kScrBytes = kConsumerWarps * kRowsPerTile * kScrStride * 4;
@@ -276,12 +333,22 @@ struct DecodeSmem {
     static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
 };
 
+__device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, D == 128 ? 2 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     using S = DecodeSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;  // set by any wait that gives up; every later wait returns at once
+    __shared__ int s_stop;   // consumers' uniform loop decision, written by consumer thread 0
+    __shared__ int s_last;   // this CTA finished a tile's last split
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *full = bar, *empty = bar + S::kStages, *qfull = bar + 2 * S::kStages, *qempty = qfull + 2;
@@ -309,64 +376,78 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) tma_prefetch_desc(&kv_map);
-        const int Hkv = a.num_kv_heads;
+        const int Hkv = a.num_kv_heads, g = a.group;
         uint32_t e = 0;  // ring element counter
-        int k = 0;       // item counter
         bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++k) {
-            const WorkItem w = a.items[it];
-            const int r = w.a.x, mt = w.a.y, h = w.a.z;
-            const int kb0 = w.b.x, kb1 = w.b.y, part = w.b.z, q0 = w.b.w;
-            const int n = w.c.x, L = w.c.y, kv_end = w.c.z;
+        int cur = 0;
+        if (lane == 0) cur = atomicAdd(&a.header->next_item, 1);
+        cur = __shfl_sync(0xffffffffu, cur, 0);
+        for (int k = 0;; ++k) {
             const int qb = k & 1;
             if (!mbar_wait(&qempty[qb], ((k >> 1) & 1) ^ 1, status, abort)) { ok = false; break; }
-            // Item description and Q rows for the consumers.
             ItemDesc &d = desc[qb];
-            const long long rows = (long long)n * a.group;
+            if (cur >= n_items) {
+                if (lane == 0) d.item = -1;
+                mbar_arrive(&qfull[qb]);
+                break;
+            }
+            const WorkItem w = a.items[cur];
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);  // next item, fetched early
+            const int r = w.a.x, mt = w.a.y, h = w.a.z, s = w.a.w;
+            const int kb0 = w.b.x, kb1 = w.b.y, q0 = w.b.w;
+            const int n = w.c.x, L = w.c.y, kv_end = w.c.z;
+            const int nv = w.d.y;
+
+            // Item description: rows (token, q head, last visible key).
             if (lane < kRowsPerTile) {
-                const long long rho = (long long)mt * kRowsPerTile + lane;
-                const bool valid = rho < rows;
-                const int i = valid ? (int)(rho / a.group) : 0;
-                const int j = valid ? (int)(rho % a.group) : 0;
+                const int rho = mt * kRowsPerTile + lane;
+                const bool valid = lane < nv;
+                const int i = valid ? rho / g : 0;
                 d.row_t[lane] = q0 + i;
-                d.row_hq[lane] = h * a.group + j;
+                d.row_hq[lane] = h * g + (valid ? rho % g : 0);
                 d.row_limit[lane] = valid ? L - n + i : kv_end - 1;
             }
             if (lane == 0) {
-                const long long nv = rows - (long long)mt * kRowsPerTile;
-                d.kb0 = kb0; d.kb1 = kb1; d.part = part;
-                d.n_valid = (int)min(nv, (long long)kRowsPerTile);
-                d.kv_end = kv_end; d.h = h;
+                d.item = cur; d.kb0 = kb0; d.kb1 = kb1; d.part_row0 = w.b.z; d.n_valid = nv;
+                d.kv_end = kv_end; d.s = s; d.ns = w.d.x; d.tile = w.c.w;
             }
+            __syncwarp();
+            // Q rows: one bulk copy per run of rows that belong to one token
+            // (consecutive q heads, contiguous in q).
             uint8_t *qs = smem + S::kOffQ + qb * S::kQBytes;
-            constexpr int kChunks = D / 8;
-#pragma unroll
-            for (int c = lane; c < kRowsPerTile * kChunks; c += 32) {
-                const int row = c / kChunks, ch = c % kChunks;
-                const long long rho = (long long)mt * kRowsPerTile + row;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (rho < rows) {
-                    const int i = (int)(rho / a.group), j = (int)(rho % a.group);
-                    const long long t = (long long)q0 + i;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        a.q + (t * a.num_q_heads + (long long)h * a.group + j) * D);
-                    val = __ldg(src + ch);
+            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], (uint32_t)nv * D * 2);
+            __syncwarp();
+            if (lane < nv) {
+                const int rho = mt * kRowsPerTile + lane;
+                const int i = rho / g;
+                const bool run_start = lane == 0 || (rho - 1) / g != i;
+                if (run_start) {
+                    int len = 1;
+                    while (lane + len < nv && (rho + len) / g == i) ++len;
+                    const __nv_bfloat16 *src = a.q + ((long long)(q0 + i) * a.num_q_heads + h * g + rho % g) * D;
+                    bulk_copy_g2s(qs + lane * S::kQStride, src, (uint32_t)len * D * 2, &qfull[qb]);
                 }
-                *reinterpret_cast<uint4 *>(qs + row * S::kQStride + ch * 16) = val;
             }
-            mbar_arrive(&qfull[qb]);
+            if (lane != 0) mbar_arrive(&qfull[qb]);
 
-            // K/V block tiles through the ring.
+            // K/V block tiles through the ring; block-table entries are
+            // fetched 32 at a time, one batch ahead.
             const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
-            for (int base = kb0; base < kb1 && ok; base += 32) {
-                int my_blk = 0;
+            auto fetch = [&](int base) {
+                int b = 0;
                 if (base + lane < kb1) {
-                    my_blk = __ldg(bt + base + lane);
-                    if (my_blk < 0 || my_blk >= a.num_blocks) {
+                    b = __ldg(bt + base + lane);
+                    if (b < 0 || b >= a.num_blocks) {
                         raise_status(status, PKV_DEV_BAD_BLOCK);
-                        my_blk = a.num_blocks;  // outside the tensor map: TMA fills zeros
+                        b = a.num_blocks;  // outside the tensor map: TMA fills zeros
                     }
                 }
+                return b;
+            };
+            int my_blk = fetch(kb0);
+            for (int base = kb0; base < kb1 && ok; base += 32) {
+                const int nxt_blk = fetch(base + 32);
                 const int cnt = min(32, kb1 - base);
                 for (int j = 0; j < cnt; ++j) {
                     const int blk = __shfl_sync(0xffffffffu, my_blk, j);
@@ -385,7 +466,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                     __syncwarp();
                     ++e;
                 }
+                my_blk = nxt_blk;
             }
+            if (!ok) break;
+            cur = __shfl_sync(0xffffffffu, nxt, 0);
         }
         // After a failure, do not leave while copies into this CTA's shared
         // memory are still in flight: wait (bounded) for the last issue of
@@ -408,13 +492,16 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     float *scr = reinterpret_cast<float *>(smem + S::kOffScr);
     float2 *sml = reinterpret_cast<float2 *>(smem + S::kOffML);
     uint32_t e = 0;
-    int k = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
+    for (int k = 0;; ++k) {
         const int qb = k & 1;
-        // Any failed wait below sets *abort; the warps still meet at both
-        // named barriers of this item and then leave together.
         const bool have_q = mbar_wait(&qfull[qb], (k >> 1) & 1, status, abort);
         const ItemDesc &d = desc[qb];
+        // One thread decides for all four warps whether to go on, so that
+        // they leave together and never strand each other at a barrier.
+        if (tid == 0) s_stop = (!have_q || *abort || d.item < 0) ? 1 : 0;
+        named_barrier_sync(1, kConsumerWarps * 32);
+        if (s_stop) return;
+
         float o[D / 8][4];
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -424,7 +511,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             const int kb0 = d.kb0, kb1 = d.kb1, kv_end = d.kv_end;
             const int lim0 = d.row_limit[qrow], lim1 = d.row_limit[qrow + 8];
 
-            // Q fragments (A operand, 16 rows x D) for the whole item.
+            // Q fragments (A operand, 16 rows x D) for the whole item. Rows
+            // past n_valid hold stale data; they only affect their own rows,
+            // which are never written.
             uint32_t qa[D / 16][4];
             {
                 const uint32_t qs = smem_u32(smem + S::kOffQ + qb * S::kQBytes);
@@ -545,8 +634,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                     mbar_arrive(&empty[stage]);
                 }
             }
-            // Keep the ring counter in step with the producer if the loop
-            // above stopped early (the CTA is aborting then anyway).
         }
 
         // Combine the four warps' states: each warp's rows -> scratch.
@@ -568,115 +655,76 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             }
         }
         named_barrier_sync(1, kConsumerWarps * 32);
-        // No wait happens between the two barriers, so every warp reads the
-        // same abort value here.
-        const bool aborted = *abort != 0;
-        if (!aborted) {
-            const int n_valid = d.n_valid, part = d.part;
-            constexpr int kC4 = D / 4;
-            for (int idx = tid; idx < kRowsPerTile * kC4; idx += kConsumerWarps * 32) {
-                const int row = idx / kC4, c4 = idx % kC4;
-                if (row >= n_valid) break;
-                float M = -INFINITY;
+        const int n_valid = d.n_valid, ns = d.ns;
+        constexpr int kC4 = D / 4;
+        const long long prow_s = (long long)d.part_row0 + (long long)d.s * n_valid;
+        for (int idx = tid; idx < n_valid * kC4; idx += kConsumerWarps * 32) {
+            const int row = idx / kC4, c4 = idx % kC4;
+            float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sml[w * kRowsPerTile + row].x);
-                float lsum = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (M != -INFINITY) {
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sml[w * kRowsPerTile + row].x);
+            float lsum = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
-                        const float2 ml = sml[w * kRowsPerTile + row];
-                        const float f = fast_exp2(ml.x - M);
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float2 ml = sml[w * kRowsPerTile + row];
+                    const float f = fast_exp2(ml.x - M);
+                    lsum += ml.y * f;
+                    const float4 v =
+                        *reinterpret_cast<const float4 *>(scr + (w * kRowsPerTile + row) * S::kScrStride + c4 * 4);
+                    acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
+                }
+            }
+            if (ns <= 1) {
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                const long long off = ((long long)d.row_t[row] * a.num_q_heads + d.row_hq[row]) * D + c4 * 4;
+                uint2 pk;
+                pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                *reinterpret_cast<uint2 *>(a.out + off) = pk;
+            } else {
+                const long long prow = prow_s + row;
+                *reinterpret_cast<float4 *>(a.part_o + prow * D + c4 * 4) = acc;
+                if (c4 == 0) a.part_ml[prow] = make_float2(M, lsum);
+            }
+        }
+        if (ns > 1) {
+            // Publish this split, then count it; the CTA that brings the
+            // count to ns merges every split of the tile (no waiting).
+            __threadfence();
+            named_barrier_sync(1, kConsumerWarps * 32);
+            if (tid == 0) s_last = atomicAdd(&a.tile_counter[d.tile], 1) == ns - 1;
+            named_barrier_sync(1, kConsumerWarps * 32);
+            if (s_last) {
+                __threadfence();
+                const long long prow0 = d.part_row0;
+                for (int idx = tid; idx < n_valid * kC4; idx += kConsumerWarps * 32) {
+                    const int row = idx / kC4, c4 = idx % kC4;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < ns; ++sp)
+                        M = fmaxf(M, __ldcg(&a.part_ml[prow0 + (long long)sp * n_valid + row]).x);
+                    float lsum = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int sp = 0; sp < ns; ++sp) {
+                        const long long prow = prow0 + (long long)sp * n_valid + row;
+                        const float2 ml = __ldcg(&a.part_ml[prow]);
+                        const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
                         lsum += ml.y * f;
-                        const float4 v = *reinterpret_cast<const float4 *>(
-                            scr + (w * kRowsPerTile + row) * S::kScrStride + c4 * 4);
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_o + prow * D + c4 * 4));
                         acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
                     }
-                }
-                if (part < 0) {
                     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
                     const long long off = ((long long)d.row_t[row] * a.num_q_heads + d.row_hq[row]) * D + c4 * 4;
                     uint2 pk;
                     pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                     pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
                     *reinterpret_cast<uint2 *>(a.out + off) = pk;
-                } else {
-                    const long long prow = (long long)part * kRowsPerTile + row;
-                    *reinterpret_cast<float4 *>(a.part_o + prow * D + c4 * 4) = acc;
-                    if (c4 == 0) a.part_ml[prow] = make_float2(M, lsum);
                 }
             }
         }
         named_barrier_sync(1, kConsumerWarps * 32);
-        if (aborted) return;
         if (lane == 0) mbar_arrive(&qempty[qb]);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// merge of split partials
-// ---------------------------------------------------------------------------
-
-struct MergeArgs {
-    __nv_bfloat16 *out;
-    const int32_t *qsl;
-    int num_reqs, num_tokens, num_q_heads, num_kv_heads, group;
-    const int32_t *req_group_base;
-    const int2 *tile_info;
-    const float2 *part_ml;
-    const float *part_o;
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row_id = (long long)blockIdx.x * 8 + warp;
-    if (row_id >= (long long)a.num_tokens * a.num_q_heads) return;
-    const int t = (int)(row_id / a.num_q_heads), hq = (int)(row_id % a.num_q_heads);
-    int lo = 0, hi = a.num_reqs;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (a.qsl[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int r = lo, q0 = a.qsl[r];
-    if (!(q0 <= t && t < a.qsl[r + 1])) return;
-    const long long rho = (long long)(t - q0) * a.group + hq % a.group;
-    const int mt = (int)(rho / kRowsPerTile), row = (int)(rho % kRowsPerTile);
-    const int g0 = a.req_group_base[r];
-    if (mt >= a.req_group_base[r + 1] - g0) return;
-    const int2 info = a.tile_info[(long long)(g0 + mt) * a.num_kv_heads + hq / a.group];
-    const int ns = info.x, pb = info.y;
-    if (ns <= 1) return;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[(long long)(pb + s) * kRowsPerTile + row].x);
-    constexpr int kPer = D / 32;
-    float acc[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-    float lsum = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const long long prow = (long long)(pb + s) * kRowsPerTile + row;
-        const float2 ml = a.part_ml[prow];
-        const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-        lsum += ml.y * f;
-        const float *src = a.part_o + prow * D + lane * kPer;
-        if constexpr (kPer == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += v.x * f; acc[1] += v.y * f; acc[2] += v.z * f; acc[3] += v.w * f;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += v.x * f; acc[1] += v.y * f;
-        }
-    }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    __nv_bfloat16 *dst = a.out + ((long long)t * a.num_q_heads + hq) * D + lane * kPer;
-    if constexpr (kPer == 4) {
-        uint2 pk;
-        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(dst) = pk;
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -686,13 +734,15 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 
 struct DeviceInfo {
     int sm_count = 0;
-    int ctas_per_sm[2] = {0, 0};  // decode kernel, D = 64 / 128
+    int ctas_per_sm[2] = {0, 0};  // attention kernel, D = 64 / 128
     bool ready = false;
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+constexpr int kPlanSmemBytes = 4 * (kPlanSmemReqs + 1) * 4;
 
 template <int D>
 int decode_occupancy() {
@@ -718,6 +768,9 @@ int device_info(DeviceInfo **out) {
         di.ctas_per_sm[0] = decode_occupancy<64>();
         di.ctas_per_sm[1] = decode_occupancy<128>();
         if (di.ctas_per_sm[0] <= 0 || di.ctas_per_sm[1] <= 0) return PKV_E_CUDA;
+        if (cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemBytes) !=
+            cudaSuccess)
+            return PKV_E_CUDA;
         if (!g_encode) {
             void *fn = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -733,9 +786,11 @@ int device_info(DeviceInfo **out) {
     return PKV_OK;
 }
 
-// Default split-KV partial capacity: enough records for kItemsPerCta items
-// per CTA of a full persistent grid.
-long long default_parts_cap(int sm_count) { return (long long)sm_count * 4 * kItemsPerCta; }
+// Default split-KV partial capacity in rows: twice a full persistent grid's
+// worth of split items (up to 3 CTAs per SM), each with a full 16-row tile.
+long long default_part_rows_cap(int sm_count) {
+    return (long long)sm_count * 3 * kItemsPerCta * kRowsPerTile * 2;
+}
 
 int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &d) {
     const cuuint64_t rows_per_block = 2ull * d.num_kv_heads * PKV_BLOCK_SIZE;
@@ -748,43 +803,6 @@ int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
 }
-
-}  // namespace
-}  // namespace pkv
-
-using namespace pkv;
-
-extern "C" PKV_API int paged_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
-                                                       int32_t num_q_heads, const pkv_cache_desc *desc,
-                                                       size_t *bytes) {
-    if (!desc || !bytes) return PKV_E_NULL;
-    int rc = check_cache_desc(*desc, /*attention=*/true);
-    if (rc) return rc;
-    if (max_num_reqs < 0 || max_num_tokens < 0) return PKV_E_DIMS;
-    if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads != 0) return PKV_E_GQA;
-    DeviceInfo *di = nullptr;
-    rc = device_info(&di);
-    if (rc) return rc;
-    const WsLayout L = ws_layout(max_num_reqs, max_num_tokens, num_q_heads, desc->num_kv_heads, desc->head_size,
-                                 default_parts_cap(di->sm_count));
-    *bytes = L.total;
-    return PKV_OK;
-}
-
-extern "C" PKV_API int paged_attention_min_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
-                                                           int32_t num_q_heads, const pkv_cache_desc *desc,
-                                                           size_t *bytes) {
-    if (!desc || !bytes) return PKV_E_NULL;
-    int rc = check_cache_desc(*desc, /*attention=*/true);
-    if (rc) return rc;
-    if (max_num_reqs < 0 || max_num_tokens < 0) return PKV_E_DIMS;
-    if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads != 0) return PKV_E_GQA;
-    *bytes = ws_layout(max_num_reqs, max_num_tokens, num_q_heads, desc->num_kv_heads, desc->head_size, 0).total;
-    return PKV_OK;
-}
-
-namespace pkv {
-namespace {
 
 void record(void *const *events, int i, cudaStream_t st) {
     if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
@@ -815,12 +833,11 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     rc = device_info(&di);
     if (rc) return rc;
     // Largest partial capacity (up to the default) that fits the workspace.
-    long long parts_cap = default_parts_cap(di->sm_count);
-    const size_t per_part = sizeof(WorkItem) + kRowsPerTile * (sizeof(float2) + sizeof(float) * D);
+    long long part_rows = default_part_rows_cap(di->sm_count);
     const size_t spare = workspace_bytes - base.total;
-    const long long fit = spare > 1024 ? (long long)((spare - 1024) / per_part) : 0;
-    if (fit < parts_cap) parts_cap = fit;
-    const WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, Hkv, D, parts_cap);
+    const long long fit = spare > 1024 ? (long long)((spare - 1024) / part_row_bytes(D)) : 0;
+    if (fit < part_rows) part_rows = fit;
+    const WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, Hkv, D, part_rows);
     if (L.total > workspace_bytes) return PKV_E_WORKSPACE;
 
     CUtensorMap kv_map;
@@ -840,17 +857,20 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.max_blocks_per_req = max_blocks_per_req;
     pa.group = num_q_heads / Hkv;
     pa.num_kv_heads = Hkv;
+    pa.block_bytes_kv = 2 * PKV_BLOCK_SIZE * D * 2;
     pa.target_items = (long long)ctas * kItemsPerCta;
-    pa.parts_cap = L.parts_cap;
+    pa.part_rows_cap = L.part_rows_cap;
     pa.groups_cap = L.groups_cap;
     pa.items_cap = L.items_cap;
     pa.header = header;
-    pa.req_group_base = reinterpret_cast<int32_t *>(ws + L.req_group_base);
+    pa.req_cache = reinterpret_cast<int32_t *>(ws + L.req_cache);
+    pa.group_req = reinterpret_cast<int32_t *>(ws + L.group_req);
     pa.group_kvb = reinterpret_cast<int32_t *>(ws + L.group_kvb);
-    pa.tile_info = reinterpret_cast<int2 *>(ws + L.tile_info);
+    pa.tile_counter = reinterpret_cast<int32_t *>(ws + L.tile_counter);
     pa.items = reinterpret_cast<WorkItem *>(ws + L.items);
+    const int plan_smem = num_reqs <= kPlanSmemReqs ? 4 * (num_reqs + 1) * 4 : 0;
     record(events, 0, st);
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
+    plan_kernel<<<1, kPlanThreads, plan_smem, st>>>(pa);
 
     DecodeArgs da;
     da.q = static_cast<const __nv_bfloat16 *>(q);
@@ -864,36 +884,51 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     da.scale_log2 = scale * kLog2e;
     da.items = pa.items;
     da.header = header;
+    da.tile_counter = pa.tile_counter;
     da.part_ml = reinterpret_cast<float2 *>(ws + L.part_ml);
     da.part_o = reinterpret_cast<float *>(ws + L.part_o);
-
-    MergeArgs ma;
-    ma.out = da.out;
-    ma.qsl = query_start_loc;
-    ma.num_reqs = num_reqs;
-    ma.num_tokens = num_tokens;
-    ma.num_q_heads = num_q_heads;
-    ma.num_kv_heads = Hkv;
-    ma.group = da.group;
-    ma.req_group_base = pa.req_group_base;
-    ma.tile_info = pa.tile_info;
-    ma.part_ml = da.part_ml;
-    ma.part_o = da.part_o;
-    const long long rows = (long long)num_tokens * num_q_heads;
-    const unsigned merge_blocks = (unsigned)((rows + 7) / 8);
 
     record(events, 1, st);
     if (D == 128) decode_kernel<128><<<ctas, kDecodeThreads, DecodeSmem<128>::kAlloc, st>>>(kv_map, da);
     else decode_kernel<64><<<ctas, kDecodeThreads, DecodeSmem<64>::kAlloc, st>>>(kv_map, da);
     record(events, 2, st);
-    if (D == 128) merge_kernel<128><<<merge_blocks, 256, 0, st>>>(ma);
-    else merge_kernel<64><<<merge_blocks, 256, 0, st>>>(ma);
     record(events, 3, st);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 }  // namespace
 }  // namespace pkv
+
+using namespace pkv;
+
+extern "C" PKV_API int paged_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
+                                                       int32_t num_q_heads, const pkv_cache_desc *desc,
+                                                       size_t *bytes) {
+    if (!desc || !bytes) return PKV_E_NULL;
+    int rc = check_cache_desc(*desc, /*attention=*/true);
+    if (rc) return rc;
+    if (max_num_reqs < 0 || max_num_tokens < 0) return PKV_E_DIMS;
+    if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads != 0) return PKV_E_GQA;
+    DeviceInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc) return rc;
+    const WsLayout L = ws_layout(max_num_reqs, max_num_tokens, num_q_heads, desc->num_kv_heads, desc->head_size,
+                                 default_part_rows_cap(di->sm_count));
+    *bytes = L.total;
+    return PKV_OK;
+}
+
+extern "C" PKV_API int paged_attention_min_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
+                                                           int32_t num_q_heads, const pkv_cache_desc *desc,
+                                                           size_t *bytes) {
+    if (!desc || !bytes) return PKV_E_NULL;
+    int rc = check_cache_desc(*desc, /*attention=*/true);
+    if (rc) return rc;
+    if (max_num_reqs < 0 || max_num_tokens < 0) return PKV_E_DIMS;
+    if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads != 0) return PKV_E_GQA;
+    *bytes = ws_layout(max_num_reqs, max_num_tokens, num_q_heads, desc->num_kv_heads, desc->head_size, 0).total;
+    return PKV_OK;
+}
 
 extern "C" PKV_API int paged_attention(const void *q, int32_t num_tokens, int32_t num_q_heads, const void *kv_cache,
                                        const pkv_cache_desc *desc, const int32_t *block_table, int32_t num_reqs,

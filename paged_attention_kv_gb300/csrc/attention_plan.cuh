@@ -5,14 +5,17 @@
 // query head h * g + rho % g. Rows are cut into tiles of 16 (mma M).
 //
 // Groups and tiles. A group is one (request, row tile mt); it expands into
-// Hkv tiles (one per kv head). req_group_base[r] is the first group of
-// request r (an exclusive prefix sum of the per-request tile counts).
+// Hkv tiles (one per kv head).
 //
 // Items. A tile's keys [0, kv_end) are cut into splits of split_blocks
 // blocks; each (tile, split) is one work item for one CTA. A tile with one
-// split writes `out` directly; a tile with several writes one partial
-// (unnormalised O, running max m in log2 units, sum l) per split, merged by
-// the merge kernel with weights 2^(m_s - max_s m_s).
+// split writes `out` directly. A tile with ns > 1 splits writes, per split,
+// its n_valid rows of (unnormalised O, running max m in log2 units, sum l)
+// to the partial rows [part_row0 + s * n_valid, ...); the CTA that finishes
+// the tile's last split (a per-tile arrival counter) merges them with
+// weights 2^(m_s - max_s m_s). Items are listed longest first (full-size
+// splits, then the shorter ones in size buckets) and handed out through an
+// atomic counter.
 #pragma once
 
 #include <cstddef>
@@ -21,49 +24,69 @@
 namespace pkv {
 
 constexpr int kRowsPerTile = 16;
+#ifndef PKV_MIN_ITEM_KB
+#define PKV_MIN_ITEM_KB 256
+#endif
+#ifndef PKV_ITEMS_PER_CTA
+#define PKV_ITEMS_PER_CTA 4
+#endif
 constexpr int kMinSplitBlocks = 4;   // at least one block per consumer warp
-constexpr int kItemsPerCta = 16;     // split target: items per persistent CTA
+// Split target. Each item ends with a CTA-wide combine whose latency idles
+// the CTA's HBM stream, so fewer, longer items win as long as the longest-
+// first order still balances the grid (a sweep on GB300 put the best at ~4
+// items per CTA and >= 256 KiB of K+V per item).
+constexpr int kMinItemBytes = PKV_MIN_ITEM_KB << 10;  // at least this much K+V per item
+constexpr int kItemsPerCta = PKV_ITEMS_PER_CTA;      // items per persistent CTA
+constexpr int kPlanSmemReqs = 4096;  // per-request tables kept in shared memory up to this many requests
+constexpr int kSizeBuckets = 9;      // 0 = full-size split, 1..8 = shorter, longest first
 
 struct WsHeader {
     int32_t status;        // device status word (first 4 bytes of the workspace)
     int32_t n_items;
     int32_t split_blocks;
     int32_t n_groups;
-    int32_t n_partials;
-    int32_t pad[59];
+    int32_t n_partial_rows;
+    int32_t next_item;     // dynamic scheduling counter
+    int32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// One work item: a = {r, mt, h, s}, b = {kb0, kb1, partial or -1, qstart},
-// c = {n, L, kv_end, 0}. kv_end is the tile's last visible key + 1.
+// a = {r, mt, h, s}, b = {kb0, kb1, part_row0 or -1, qstart},
+// c = {n, L, kv_end, tile}, d = {ns, n_valid, 0, 0}.
 struct WorkItem {
-    int4 a, b, c;
+    int4 a, b, c, d;
 };
 
 struct WsLayout {
-    size_t req_group_base, group_kvb, tile_info, items, part_ml, part_o, total;
-    long long groups_cap, tiles_cap, items_cap, parts_cap;
+    size_t req_cache, group_req, group_kvb, tile_counter, items, part_ml, part_o, total;
+    long long groups_cap, tiles_cap, items_cap, part_rows_cap;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WsLayout ws_layout(long long num_reqs, long long num_tokens, int num_q_heads, int num_kv_heads,
-                          int head_size, long long parts_cap) {
+                          int head_size, long long part_rows_cap) {
     WsLayout L{};
     const long long g = num_q_heads / num_kv_heads;
     L.groups_cap = (num_tokens * g + kRowsPerTile - 1) / kRowsPerTile + num_reqs;
     L.tiles_cap = L.groups_cap * num_kv_heads;
-    L.parts_cap = parts_cap;
-    L.items_cap = L.tiles_cap + parts_cap;
+    L.part_rows_cap = part_rows_cap;
+    L.items_cap = L.tiles_cap + part_rows_cap;
     size_t off = sizeof(WsHeader);
-    L.req_group_base = off; off = align256(off + sizeof(int32_t) * (num_reqs + 1));
-    L.group_kvb = off;      off = align256(off + sizeof(int32_t) * L.groups_cap);
-    L.tile_info = off;      off = align256(off + sizeof(int2) * L.tiles_cap);
-    L.items = off;          off = align256(off + sizeof(WorkItem) * L.items_cap);
-    L.part_ml = off;        off = align256(off + sizeof(float2) * kRowsPerTile * parts_cap);
-    L.part_o = off;         off = align256(off + sizeof(float) * kRowsPerTile * head_size * parts_cap);
+    L.req_cache = off;    off = align256(off + sizeof(int32_t) * 4 * (num_reqs + 1));
+    L.group_req = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
+    L.group_kvb = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
+    L.tile_counter = off; off = align256(off + sizeof(int32_t) * L.tiles_cap);
+    L.items = off;        off = align256(off + sizeof(WorkItem) * L.items_cap);
+    L.part_ml = off;      off = align256(off + sizeof(float2) * part_rows_cap);
+    L.part_o = off;       off = align256(off + sizeof(float) * head_size * part_rows_cap);
     L.total = off;
     return L;
+}
+
+// Bytes per partial row (item slot, m/l pair, O row) used to size capacity.
+inline size_t part_row_bytes(int head_size) {
+    return sizeof(WorkItem) + sizeof(float2) + sizeof(float) * head_size;
 }
 
 }  // namespace pkv
