@@ -25,6 +25,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "attention_chunk.h"
 #include "attention_plan.cuh"
 #include "pagedkv.h"
 #include "pkv_device.cuh"
@@ -47,13 +48,15 @@ struct PlanArgs {
     const int32_t *seq_lens;
     int num_reqs, num_tokens, max_blocks_per_req, group, num_kv_heads;
     int block_bytes_kv;  // K + V bytes of one (block, kv head): 2 * 16 * D * 2
-    long long target_items, part_rows_cap, groups_cap, items_cap;
+    int chunk_ok;        // the tcgen05 chunk kernel can take this shape (128 % g == 0)
+    long long target_items, part_rows_cap, groups_cap, items_cap, chunk_items_cap;
     WsHeader *header;
-    int32_t *req_cache;  // 4 * (num_reqs + 1) ints, used when the batch has too many requests for shared memory
+    int32_t *req_cache;  // kReqCacheArrays * (num_reqs + 1) ints, when the batch has too many requests for shared memory
     int32_t *group_req;
     int32_t *group_kvb;
     int32_t *tile_counter;
     WorkItem *items;
+    ChunkItem *chunk_items;
 };
 
 // Exclusive scan over the 1024 threads of the block; *total gets the sum.
@@ -132,10 +135,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int stride = R + 1;
     int32_t *cache = R <= kPlanSmemReqs ? s_req : a.req_cache;
     int32_t *req_n = cache, *req_L = cache + stride, *req_q0 = cache + 2 * stride, *req_g = cache + 3 * stride;
+    int32_t *req_c = cache + 4 * stride;  // first chunk tile of each request
+    __shared__ int s_kvmax;
 
     if (tid == 0) {
         a.header->status = 0;
         a.header->next_item = 0;
+        a.header->next_chunk_item = 0;
+        s_kvmax = 0;
         if (a.qsl[0] != 0 || a.qsl[R] != a.num_tokens) atomicOr(status, PKV_DEV_BAD_QSL);
     }
     if (tid < kSizeBuckets) {
@@ -145,10 +152,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __syncthreads();
 
     // 1. validate requests, cache (n, L, q0), tiles per request -> group base.
-    int carry = 0;
+    // Requests with at least kChunkRows query rows go to the chunk kernel.
+    int carry = 0, ccarry = 0;
     for (int base = 0; base < R; base += kPlanThreads) {
         const int r = base + tid;
-        int mtiles = 0;
+        int mtiles = 0, ctiles = 0;
         if (r < R) {
             const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
             const int n = q1 - q0;
@@ -159,17 +167,34 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
                 atomicOr(status, PKV_DEV_BAD_LEN);
             } else {
                 ok = true;
-                mtiles = (int)(((long long)n * g + kRowsPerTile - 1) / kRowsPerTile);
+                const long long rows = (long long)n * g;
+                if (a.chunk_ok && rows >= kChunkRows)
+                    ctiles = (int)((rows + kChunkRows - 1) / kChunkRows);
+                else
+                    mtiles = (int)((rows + kRowsPerTile - 1) / kRowsPerTile);
             }
             req_n[r] = ok ? n : 0;
             req_L[r] = L;
             req_q0[r] = q0;
         }
-        int chunk_total;
+        int chunk_total, ctotal;
         const int ex = block_exclusive_scan<int>(mtiles, &chunk_total, s_i);
-        if (r < R) req_g[r] = carry + ex;
+        const int cex = block_exclusive_scan<int>(ctiles, &ctotal, s_i);
+        if (r < R) {
+            req_g[r] = carry + ex;
+            req_c[r] = ccarry + cex;
+        }
         carry += chunk_total;
+        ccarry += ctotal;
     }
+    int n_cgroups = ccarry;
+    if ((long long)n_cgroups * Hkv > a.chunk_items_cap) {  // only overlapping query_start_loc ranges
+        if (tid == 0) atomicOr(status, PKV_DEV_OVERFLOW);
+        n_cgroups = (int)(a.chunk_items_cap / Hkv);
+        __syncthreads();
+        for (int r = tid; r < R; r += kPlanThreads) req_c[r] = min(req_c[r], n_cgroups);
+    }
+    if (tid == 0) req_c[R] = n_cgroups;
     int n_groups = carry;
     if (n_groups > a.groups_cap) {
         // Only overlapping (invalid) query_start_loc ranges get here: keep
@@ -283,6 +308,57 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.header->split_blocks = split;
         a.header->n_groups = n_groups;
         a.header->n_partial_rows = row_carry;
+    }
+
+    // 6. chunk items, longest first: 8 buckets of kv_end below the maximum.
+    __syncthreads();
+    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
+        const int r = find_group_request(req_c, R, gi);
+        const int mt = gi - req_c[r];
+        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
+        atomicMax(&s_kvmax, req_L[r] - req_n[r] + (int)(last_row / g) + 1);
+    }
+    if (tid < kSizeBuckets) {
+        s_bucket_count[tid] = 0;
+        s_bucket_cursor[tid] = 0;
+    }
+    __syncthreads();
+    const int kvmax = s_kvmax;
+    auto chunk_bucket = [&](int kv_end) {
+        return min(kSizeBuckets - 1, (int)((long long)(kvmax - kv_end) * (kSizeBuckets - 1) / (kvmax + 1)));
+    };
+    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
+        const int r = find_group_request(req_c, R, gi);
+        const int mt = gi - req_c[r];
+        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
+        atomicAdd(&s_bucket_count[chunk_bucket(req_L[r] - req_n[r] + (int)(last_row / g) + 1)], Hkv);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int b = 0; b < kSizeBuckets; ++b) {
+            s_bucket_base[b] = acc;
+            acc += s_bucket_count[b];
+        }
+        a.header->n_chunk_items = acc;
+    }
+    __syncthreads();
+    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
+        const int r = find_group_request(req_c, R, gi);
+        const int mt = gi - req_c[r];
+        const int n = req_n[r], L = req_L[r];
+        const long long rows = (long long)n * g;
+        const long long last_row = min(rows - 1, (long long)mt * kChunkRows + kChunkRows - 1);
+        const int kv_end = L - n + (int)(last_row / g) + 1;
+        const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
+        const int b = chunk_bucket(kv_end);
+        for (int h = 0; h < Hkv; ++h) {
+            const int idx = s_bucket_base[b] + atomicAdd(&s_bucket_cursor[b], 1);
+            ChunkItem c;
+            c.a = make_int4(r, mt, h, kv_end);
+            c.b = make_int4(req_q0[r], n, L, nv);
+            a.chunk_items[idx] = c;
+        }
     }
 }
 
@@ -742,7 +818,7 @@ std::mutex g_mu;
 DeviceInfo g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kPlanSmemBytes = 4 * (kPlanSmemReqs + 1) * 4;
+constexpr int kPlanSmemBytes = kReqCacheArrays * (kPlanSmemReqs + 1) * 4;
 
 template <int D>
 int decode_occupancy() {
@@ -771,6 +847,7 @@ int device_info(DeviceInfo **out) {
         if (cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemBytes) !=
             cudaSuccess)
             return PKV_E_CUDA;
+        if (chunk_configure() != PKV_OK) return PKV_E_CUDA;
         if (!g_encode) {
             void *fn = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -800,6 +877,19 @@ int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv_cache), dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
+}
+
+// q [T][Hq][D] as a 3-D map; one box is the 128 rows of a chunk tile: 128/g
+// tokens x the g q heads of one kv head x 64 columns.
+int encode_q_map(CUtensorMap *map, const void *q, int num_tokens, int num_q_heads, int head_size, int group) {
+    cuuint64_t dims[3] = {(cuuint64_t)head_size, (cuuint64_t)num_q_heads, (cuuint64_t)num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)head_size * 2, (cuuint64_t)num_q_heads * head_size * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(kChunkRows / group)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
 }
@@ -843,6 +933,15 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     CUtensorMap kv_map;
     rc = encode_kv_map(&kv_map, kv_cache, *desc);
     if (rc) return rc;
+    const int group = num_q_heads / Hkv;
+    // The chunk kernel takes requests with >= 128 query rows when a 128-row
+    // tile holds whole tokens.
+    const bool chunk_ok = kChunkRows % group == 0 && (long long)num_tokens * group >= kChunkRows;
+    CUtensorMap q_map;
+    if (chunk_ok) {
+        rc = encode_q_map(&q_map, q, num_tokens, num_q_heads, D, group);
+        if (rc) return rc;
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -858,6 +957,9 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.group = num_q_heads / Hkv;
     pa.num_kv_heads = Hkv;
     pa.block_bytes_kv = 2 * PKV_BLOCK_SIZE * D * 2;
+    pa.chunk_ok = chunk_ok ? 1 : 0;
+    pa.chunk_items_cap = L.chunk_items_cap;
+    pa.chunk_items = reinterpret_cast<ChunkItem *>(ws + L.chunk_items);
     pa.target_items = (long long)ctas * kItemsPerCta;
     pa.part_rows_cap = L.part_rows_cap;
     pa.groups_cap = L.groups_cap;
@@ -868,7 +970,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.group_kvb = reinterpret_cast<int32_t *>(ws + L.group_kvb);
     pa.tile_counter = reinterpret_cast<int32_t *>(ws + L.tile_counter);
     pa.items = reinterpret_cast<WorkItem *>(ws + L.items);
-    const int plan_smem = num_reqs <= kPlanSmemReqs ? 4 * (num_reqs + 1) * 4 : 0;
+    const int plan_smem = num_reqs <= kPlanSmemReqs ? kReqCacheArrays * (num_reqs + 1) * 4 : 0;
     record(events, 0, st);
     plan_kernel<<<1, kPlanThreads, plan_smem, st>>>(pa);
 
@@ -888,6 +990,20 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     da.part_ml = reinterpret_cast<float2 *>(ws + L.part_ml);
     da.part_o = reinterpret_cast<float *>(ws + L.part_o);
 
+    if (chunk_ok) {
+        ChunkArgs ca;
+        ca.block_table = block_table;
+        ca.max_blocks_per_req = max_blocks_per_req;
+        ca.num_blocks = desc->num_blocks;
+        ca.num_q_heads = num_q_heads;
+        ca.num_kv_heads = Hkv;
+        ca.group = group;
+        ca.scale_log2 = scale * kLog2e;
+        ca.items = pa.chunk_items;
+        ca.header = header;
+        ca.out = static_cast<__nv_bfloat16 *>(out);
+        chunk_launch(D, di->sm_count, kv_map, q_map, ca, st);
+    }
     record(events, 1, st);
     if (D == 128) decode_kernel<128><<<ctas, kDecodeThreads, DecodeSmem<128>::kAlloc, st>>>(kv_map, da);
     else decode_kernel<64><<<ctas, kDecodeThreads, DecodeSmem<64>::kAlloc, st>>>(kv_map, da);

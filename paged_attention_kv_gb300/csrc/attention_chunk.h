@@ -1,0 +1,33 @@
+// Interface between the attention host code and the tcgen05 chunk kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attention_plan.cuh"
+
+namespace pkv {
+
+// a = {r, row tile mt (128 rows), kv head h, kv_end}, b = {qstart, n, L, valid rows}.
+struct ChunkItem {
+    int4 a, b;
+};
+
+struct ChunkArgs {
+    const int32_t *block_table;
+    int max_blocks_per_req, num_blocks, num_q_heads, num_kv_heads, group;
+    float scale_log2;
+    const ChunkItem *items;
+    WsHeader *header;
+    __nv_bfloat16 *out;
+};
+
+int chunk_smem_bytes(int head_size);
+int chunk_configure();  // kernel attributes; once per device
+void chunk_launch(int head_size, int grid, const CUtensorMap &kv_map, const CUtensorMap &q_map, const ChunkArgs &args,
+                  cudaStream_t stream);
+
+}  // namespace pkv

@@ -40,6 +40,11 @@ constexpr int kItemsPerCta = PKV_ITEMS_PER_CTA;      // items per persistent CTA
 constexpr int kPlanSmemReqs = 4096;  // per-request tables kept in shared memory up to this many requests
 constexpr int kSizeBuckets = 9;      // 0 = full-size split, 1..8 = shorter, longest first
 
+// Chunk tiles (tcgen05 path): requests with at least kChunkRows query rows
+// (n * g) are cut into 128-row tiles that run over 128-key tiles.
+constexpr int kChunkRows = 128;
+constexpr int kChunkKeys = 128;
+
 struct WsHeader {
     int32_t status;        // device status word (first 4 bytes of the workspace)
     int32_t n_items;
@@ -47,7 +52,9 @@ struct WsHeader {
     int32_t n_groups;
     int32_t n_partial_rows;
     int32_t next_item;     // dynamic scheduling counter
-    int32_t pad[58];
+    int32_t n_chunk_items;
+    int32_t next_chunk_item;
+    int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -58,9 +65,11 @@ struct WorkItem {
 };
 
 struct WsLayout {
-    size_t req_cache, group_req, group_kvb, tile_counter, items, part_ml, part_o, total;
-    long long groups_cap, tiles_cap, items_cap, part_rows_cap;
+    size_t req_cache, group_req, group_kvb, tile_counter, items, chunk_items, part_ml, part_o, total;
+    long long groups_cap, tiles_cap, items_cap, chunk_items_cap, part_rows_cap;
 };
+
+constexpr int kReqCacheArrays = 5;  // n, L, q0, decode-tile base, chunk-tile base
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -72,12 +81,14 @@ inline WsLayout ws_layout(long long num_reqs, long long num_tokens, int num_q_he
     L.tiles_cap = L.groups_cap * num_kv_heads;
     L.part_rows_cap = part_rows_cap;
     L.items_cap = L.tiles_cap + part_rows_cap;
+    L.chunk_items_cap = ((num_tokens * g + kChunkRows - 1) / kChunkRows + num_reqs) * num_kv_heads;
     size_t off = sizeof(WsHeader);
-    L.req_cache = off;    off = align256(off + sizeof(int32_t) * 4 * (num_reqs + 1));
+    L.req_cache = off;    off = align256(off + sizeof(int32_t) * kReqCacheArrays * (num_reqs + 1));
     L.group_req = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
     L.group_kvb = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
     L.tile_counter = off; off = align256(off + sizeof(int32_t) * L.tiles_cap);
     L.items = off;        off = align256(off + sizeof(WorkItem) * L.items_cap);
+    L.chunk_items = off;  off = align256(off + 32 * L.chunk_items_cap);
     L.part_ml = off;      off = align256(off + sizeof(float2) * part_rows_cap);
     L.part_o = off;       off = align256(off + sizeof(float) * head_size * part_rows_cap);
     L.total = off;

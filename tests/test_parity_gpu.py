@@ -217,3 +217,18 @@ def test_empty_batch_is_a_no_op():
     qsl = torch.zeros(2, dtype=torch.int32, device="cuda")
     out = pkv.paged_attention(q, pool, bt, sl, qsl, 0.1)
     assert out.numel() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (32, 4, 64), (32, 32, 128), (32, 2, 64), (32, 1, 128),
+                                      (16, 16, 64), (40, 5, 128)])
+def test_chunk_tiles_across_gqa_groups(hq, hkv, d):
+    """Requests with at least 128 query rows (tokens x GQA group) run as
+    128-row tensor-core chunk tiles: ragged last tiles, chunks at an offset,
+    fresh prompts, mixed with decode tokens in one batch."""
+    shape = wl.ModelShape(f"chunk-h{hq}-{hkv}-{d}", hq, hkv, d)
+    g = hq // hkv
+    n_big = max(200 // g, 129 // g + 1)
+    seq = [n_big, 700 + n_big, 3 * n_big + 5, 300, 64]
+    ql = [n_big, n_big, 2 * n_big + 1, 1, 3]
+    batch = _custom(shape, seq, ql, 200 + hq + hkv + d)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
