@@ -39,7 +39,14 @@ METRIC = "decode attention tokens/s and achieved HBM GB/s (fraction of GB300 pea
 UNIT = "tokens/s"
 KERNEL_SOURCES = ("attention.cu", "attention_plan.cuh", "pkv_device.cuh")
 PROFILE_DOC = os.path.join(REPO, "profiles", "attention_decode_kernel_llama8b.md")
-LAUNCHES_PER_STEP = 4  # slot mapping, KV write, work list, attention (split merge folded in)
+KERNEL_SOURCES_CHUNK = ("attention_chunk.cu", "attention_chunk.h", "attention_plan.cuh", "pkv_device.cuh")
+
+
+def launches_per_step(batch) -> int:
+    """Slot mapping, KV write, work list, split-KV attention, and the chunk-tile
+    kernel whenever a 128-row tile can hold whole tokens of the batch."""
+    g = batch.shape.num_q_heads // batch.shape.num_kv_heads
+    return 4 + (1 if 128 % g == 0 and batch.num_tokens * g >= 128 else 0)
 
 
 def parse_args():
@@ -73,14 +80,39 @@ def workload_config(batch) -> dict:
     }
 
 
-def algorithmic_bytes(batch) -> dict:
+def chunk_requests(batch) -> np.ndarray:
+    """Requests the chunk-tile kernel takes: >= 128 query rows (new tokens x
+    GQA group) when a 128-row tile holds whole tokens."""
+    g = batch.shape.num_q_heads // batch.shape.num_kv_heads
+    if 128 % g != 0 or batch.num_tokens * g < 128:
+        return np.zeros(batch.num_reqs, dtype=bool)
+    return batch.query_lens.astype(np.int64) * g >= 128
+
+
+def chunk_flops(batch) -> float:
+    """Causal-exact flops of the chunk tiles: 4 * D per (query row, visible key)."""
+    s = batch.shape
+    g = s.num_q_heads // s.num_kv_heads
+    total = 0
+    for r in np.nonzero(chunk_requests(batch))[0]:
+        n, L = int(batch.query_lens[r]), int(batch.seq_lens[r])
+        visible = np.arange(L - n + 1, L + 1, dtype=np.int64).sum()
+        total += 4 * s.head_size * g * s.num_kv_heads * int(visible)
+    return float(total)
+
+
+def algorithmic_bytes(batch, only=None) -> dict:
     """Bytes one attention launch must move at minimum: every context
     token's K and V once (blocks shared by several requests counted once),
     Q read, output written, the block-table entries used and the per-request
-    metadata."""
+    metadata. `only`: a boolean mask of the requests to count (one kernel's
+    share)."""
     s = batch.shape
+    sel = np.ones(batch.num_reqs, dtype=bool) if only is None else np.asarray(only)
     rows_used = {}
     for r, L in enumerate(batch.seq_lens):
+        if not sel[r]:
+            continue
         L = int(L)
         nb = -(-L // 16)
         for j in range(nb):
@@ -91,10 +123,10 @@ def algorithmic_bytes(batch) -> dict:
     unique_tokens = sum(rows_used.values())
     per_token = 2 * s.num_kv_heads * s.head_size * 2
     kv = unique_tokens * per_token
-    logical_kv = int(batch.seq_lens.sum()) * per_token
-    qo = 2 * batch.num_tokens * s.num_q_heads * s.head_size * 2
-    bt = int(sum(-(-int(L) // 16) for L in batch.seq_lens)) * 4
-    meta = (2 * batch.num_reqs + 1) * 4
+    logical_kv = int(batch.seq_lens[sel].sum()) * per_token
+    qo = 2 * int(batch.query_lens[sel].sum()) * s.num_q_heads * s.head_size * 2
+    bt = int(sum(-(-int(L) // 16) for L in batch.seq_lens[sel])) * 4
+    meta = (2 * int(sel.sum()) + 1) * 4
     return {"kv": kv, "logical_kv": logical_kv, "q_out": qo, "block_table": bt, "meta": meta,
             "attention_total": kv + qo + bt + meta, "unique_tokens": unique_tokens}
 
@@ -125,9 +157,19 @@ def measured_peaks() -> dict:
     try:
         with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
     except (OSError, KeyError, ValueError):
-        return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def chunk_roofline(batch, chunk_ms: float, peaks: dict) -> dict:
+    """The chunk-tile kernel against the bf16 tensor peak (a contraction)."""
+    fl = chunk_flops(batch)
+    achieved = fl / (chunk_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": "chunk_kernel (tcgen05)", "achieved": achieved,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+            "flops_per_launch": fl, "kernel_us": chunk_ms * 1e3, "traffic": None}
 
 
 # --------------------------------------------------------------------------
@@ -370,7 +412,9 @@ def main():
         raise RuntimeError(f"device status bits set: {st:#x} {wst:#x}")
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
-    attn_ms = [e4[1].elapsed_time(e4[2]) for e4 in ev]
+    plan_ms = float(np.mean([e4[0].elapsed_time(e4[1]) for e4 in ev]))
+    chunk_ms = float(np.mean([e4[1].elapsed_time(e4[2]) for e4 in ev]))
+    attn_ms = [e4[2].elapsed_time(e4[3]) for e4 in ev]
     attn_call_ms = [e4[0].elapsed_time(e4[3]) for e4 in ev]
     kernel_ms = float(np.mean(attn_ms))
 
@@ -388,7 +432,9 @@ def main():
             dist.destroy_process_group()
         return
 
-    ab = algorithmic_bytes(batch)
+    chunk_mask = chunk_requests(batch)
+    ab = algorithmic_bytes(batch, only=~chunk_mask)   # what the split-KV kernel reads and writes
+    ab_all = algorithmic_bytes(batch)
     peaks = measured_peaks()
     achieved = ab["attention_total"] / (kernel_ms * 1e-3) / 1e9
     ms_per_step = elapsed_ms / args.steps
@@ -406,11 +452,13 @@ def main():
                      "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": ab["attention_total"],
                      "kernel_us": kernel_ms * 1e3, "attention_call_us": float(np.mean(attn_call_ms)) * 1e3,
                      "frac_of_8tbps_nominal": achieved / 8000.0},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "kernels_us": {"work_list": plan_ms * 1e3, "chunk_tiles": chunk_ms * 1e3, "split_kv": kernel_ms * 1e3},
+        "roofline_chunk_tiles": chunk_roofline(batch, chunk_ms, peaks) if chunk_mask.any() else None,
+        "gpu_launches": launches_per_step(batch) * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "kv_bytes_per_step": {"unique": ab["kv"], "logical": ab["logical_kv"]},
+        "kv_bytes_per_step": {"unique": ab_all["kv"], "logical": ab_all["logical_kv"]},
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -179,9 +179,10 @@ int paged_attention(const void *q, int32_t num_tokens, int32_t num_q_heads,
 /*
  * paged_attention, plus CUDA events recorded on `stream` between its
  * launches, for measuring each kernel on the stream it runs on: events[0]
- * before the work-list kernel, events[1] before the attention kernel (which
- * also merges split partials), events[2] after it, events[3] at the end of
- * the call.
+ * before the work-list kernel, events[1] after it, events[2] after the
+ * chunk-tile kernel (requests with >= 128 query rows; equal to events[1]
+ * when it is not launched), events[3] after the split-KV kernel (all other
+ * rows; it also merges split partials).
  * `events` holds four cudaEvent_t handles created by the caller (a NULL
  * entry is skipped). Same arguments, results and errors as paged_attention.
  */

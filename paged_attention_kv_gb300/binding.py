@@ -189,7 +189,8 @@ def paged_attention(q, kv_cache, block_table, seq_lens, query_start_loc, scale: 
                     stream=None, events=None) -> torch.Tensor:
     """Attention over the paged pool. ``events``: optional four
     torch.cuda.Event(enable_timing=True) recorded before the work-list
-    kernel, before and after the attention kernel, and after the merge."""
+    kernel, after it, after the chunk-tile kernel and after the split-KV
+    kernel."""
     _want(q, torch.bfloat16, 3, "q")
     _want(kv_cache, torch.bfloat16, 5, "kv_cache")
     _want(block_table, torch.int32, 2, "block_table")

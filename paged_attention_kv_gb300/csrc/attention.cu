@@ -973,6 +973,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     const int plan_smem = num_reqs <= kPlanSmemReqs ? kReqCacheArrays * (num_reqs + 1) * 4 : 0;
     record(events, 0, st);
     plan_kernel<<<1, kPlanThreads, plan_smem, st>>>(pa);
+    record(events, 1, st);
 
     DecodeArgs da;
     da.q = static_cast<const __nv_bfloat16 *>(q);
@@ -1004,10 +1005,9 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.out = static_cast<__nv_bfloat16 *>(out);
         chunk_launch(D, di->sm_count, kv_map, q_map, ca, st);
     }
-    record(events, 1, st);
+    record(events, 2, st);
     if (D == 128) decode_kernel<128><<<ctas, kDecodeThreads, DecodeSmem<128>::kAlloc, st>>>(kv_map, da);
     else decode_kernel<64><<<ctas, kDecodeThreads, DecodeSmem<64>::kAlloc, st>>>(kv_map, da);
-    record(events, 2, st);
     record(events, 3, st);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
