@@ -124,41 +124,55 @@ __device__ __forceinline__ int size_bucket(int size, int split) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
-    extern __shared__ int32_t s_req[];  // 4 * (kPlanSmemReqs + 1) ints when the batch fits
+    // Dynamic shared memory: the per-request tables when the batch has at
+    // most kPlanSmemReqs requests, then the per-group tables when there are
+    // at most kPlanSmemGroups decode groups; else those live in the workspace.
+    extern __shared__ int32_t s_dyn[];
     __shared__ long long s_ll[32];
+    __shared__ unsigned long long s_ull[32];
     __shared__ int s_i[32];
-    __shared__ int s_split;
+    __shared__ int s_split, s_kvmax;
     __shared__ int s_bucket_count[kSizeBuckets], s_bucket_base[kSizeBuckets], s_bucket_cursor[kSizeBuckets];
+    __shared__ int s_cbucket_count[kSizeBuckets], s_cbucket_base[kSizeBuckets], s_cbucket_cursor[kSizeBuckets];
+    pdl_launch_dependents();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int R = a.num_reqs, Hkv = a.num_kv_heads, g = a.group;
     int32_t *status = &a.header->status;
     const int stride = R + 1;
-    int32_t *cache = R <= kPlanSmemReqs ? s_req : a.req_cache;
+    const bool req_smem = R <= kPlanSmemReqs;
+    int32_t *cache = req_smem ? s_dyn : a.req_cache;
     int32_t *req_n = cache, *req_L = cache + stride, *req_q0 = cache + 2 * stride, *req_g = cache + 3 * stride;
     int32_t *req_c = cache + 4 * stride;  // first chunk tile of each request
-    __shared__ int s_kvmax;
+    int32_t *grp_req = a.group_req, *grp_kvb = a.group_kvb;
+    if (req_smem && a.groups_cap <= kPlanSmemGroups) {
+        grp_req = s_dyn + kReqCacheArrays * stride;
+        grp_kvb = grp_req + a.groups_cap;
+    }
 
     if (tid == 0) {
         a.header->status = 0;
         a.header->next_item = 0;
         a.header->next_chunk_item = 0;
         s_kvmax = 0;
-        if (a.qsl[0] != 0 || a.qsl[R] != a.num_tokens) atomicOr(status, PKV_DEV_BAD_QSL);
     }
     if (tid < kSizeBuckets) {
-        s_bucket_count[tid] = 0;
+        s_cbucket_count[tid] = 0;
+        s_cbucket_cursor[tid] = 0;
         s_bucket_cursor[tid] = 0;
     }
     __syncthreads();
 
-    // 1. validate requests, cache (n, L, q0), tiles per request -> group base.
-    // Requests with at least kChunkRows query rows go to the chunk kernel.
-    int carry = 0, ccarry = 0;
+    // 1. validate requests, cache (n, L, q0), tiles per request. Requests
+    // with at least kChunkRows query rows go to the chunk kernel. One scan
+    // carries both tile counts (decode tiles low, chunk tiles high).
+    long long carry = 0;
     for (int base = 0; base < R; base += kPlanThreads) {
         const int r = base + tid;
-        int mtiles = 0, ctiles = 0;
+        unsigned long long tiles = 0;
         if (r < R) {
             const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
+            if ((r == 0 && q0 != 0) || (r == R - 1 && q1 != a.num_tokens)) atomicOr(status, PKV_DEV_BAD_QSL);
             const int n = q1 - q0;
             bool ok = false;
             if (n < 0 || q0 < 0 || q1 > a.num_tokens) {
@@ -168,112 +182,123 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             } else {
                 ok = true;
                 const long long rows = (long long)n * g;
-                if (a.chunk_ok && rows >= kChunkRows)
-                    ctiles = (int)((rows + kChunkRows - 1) / kChunkRows);
-                else
-                    mtiles = (int)((rows + kRowsPerTile - 1) / kRowsPerTile);
+                if (a.chunk_ok && rows >= kChunkRows) {
+                    tiles = (unsigned long long)((rows + kChunkRows - 1) / kChunkRows) << 32;
+                    atomicMax(&s_kvmax, L);
+                } else {
+                    tiles = (unsigned long long)((rows + kRowsPerTile - 1) / kRowsPerTile);
+                }
             }
             req_n[r] = ok ? n : 0;
             req_L[r] = L;
             req_q0[r] = q0;
         }
-        int chunk_total, ctotal;
-        const int ex = block_exclusive_scan<int>(mtiles, &chunk_total, s_i);
-        const int cex = block_exclusive_scan<int>(ctiles, &ctotal, s_i);
+        unsigned long long total;
+        const unsigned long long ex = block_exclusive_scan<unsigned long long>(tiles, &total, s_ull);
+        const unsigned long long c = (unsigned long long)carry + ex;
         if (r < R) {
-            req_g[r] = carry + ex;
-            req_c[r] = ccarry + cex;
+            req_g[r] = (int)(c & 0xffffffffu);
+            req_c[r] = (int)(c >> 32);
         }
-        carry += chunk_total;
-        ccarry += ctotal;
+        carry += (long long)total;
     }
-    int n_cgroups = ccarry;
-    if ((long long)n_cgroups * Hkv > a.chunk_items_cap) {  // only overlapping query_start_loc ranges
-        if (tid == 0) atomicOr(status, PKV_DEV_OVERFLOW);
-        n_cgroups = (int)(a.chunk_items_cap / Hkv);
-        __syncthreads();
-        for (int r = tid; r < R; r += kPlanThreads) req_c[r] = min(req_c[r], n_cgroups);
-    }
-    if (tid == 0) req_c[R] = n_cgroups;
-    int n_groups = carry;
-    if (n_groups > a.groups_cap) {
+    int n_groups = (int)(carry & 0xffffffff), n_cgroups = (int)((unsigned long long)carry >> 32);
+    if (n_groups > a.groups_cap || (long long)n_cgroups * Hkv > a.chunk_items_cap) {
         // Only overlapping (invalid) query_start_loc ranges get here: keep
         // every table index in bounds.
         if (tid == 0) atomicOr(status, PKV_DEV_OVERFLOW);
-        n_groups = (int)a.groups_cap;
+        n_groups = (int)min((long long)n_groups, a.groups_cap);
+        n_cgroups = (int)min((long long)n_cgroups, a.chunk_items_cap / Hkv);
         __syncthreads();
-        for (int r = tid; r < R; r += kPlanThreads) req_g[r] = min(req_g[r], n_groups);
+        for (int r = tid; r < R; r += kPlanThreads) {
+            req_g[r] = min(req_g[r], n_groups);
+            req_c[r] = min(req_c[r], n_cgroups);
+        }
     }
-    if (tid == 0) req_g[R] = n_groups;
+    if (tid == 0) {
+        req_g[R] = n_groups;
+        req_c[R] = n_cgroups;
+    }
     __syncthreads();
 
-    // 2. keys per group, total work in block loads.
+    // 2. keys per decode group, total work in block loads; chunk buckets.
     long long work = 0;
     for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
         const int r = find_group_request(req_g, R, gi);
         const int mt = gi - req_g[r];
         const int kvb = (tile_kv_end(req_n[r], req_L[r], g, mt) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-        a.group_req[gi] = r;
-        a.group_kvb[gi] = kvb;
+        grp_req[gi] = r;
+        grp_kvb[gi] = kvb;
         work += (long long)kvb * Hkv;
     }
-    work = block_sum<long long>(work, s_ll);  // (its barriers also publish group_req / group_kvb)
-
-    // 3. split length: about target_items items, partial rows within capacity.
-    if (tid == 0) {
-        long long s = (work + a.target_items - 1) / max(1LL, a.target_items);
-        s = max(s, (long long)kMinSplitBlocks);
-        s = max(s, (long long)(kMinItemBytes / a.block_bytes_kv));
-        if (a.part_rows_cap <= 0) s = INT_MAX / 2;
-        s_split = (int)min(s, (long long)(INT_MAX / 2));
+    const int kvmax = s_kvmax;
+    auto chunk_kv_end = [&](int r, int mt) {
+        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
+        return req_L[r] - req_n[r] + (int)(last_row / g) + 1;
+    };
+    auto chunk_bucket = [&](int kv_end) {  // longest first
+        return min(kSizeBuckets - 1, (int)((long long)(kvmax - kv_end) * (kSizeBuckets - 1) / (kvmax + 1)));
+    };
+    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
+        const int r = find_group_request(req_c, R, gi);
+        atomicAdd(&s_cbucket_count[chunk_bucket(chunk_kv_end(r, gi - req_c[r]))], Hkv);
     }
-    __syncthreads();
+    work = block_sum<long long>(work, s_ll);  // (its barriers also publish the group tables)
+
+    // 3. split length: about target_items items, partial rows within
+    // capacity; the same pass counts items per size bucket.
+    if (tid == 0) {
+        long long sp = (work + a.target_items - 1) / max(1LL, a.target_items);
+        sp = max(sp, (long long)kMinSplitBlocks);
+        sp = max(sp, (long long)(kMinItemBytes / a.block_bytes_kv));
+        if (a.part_rows_cap <= 0) sp = INT_MAX / 2;
+        s_split = (int)min(sp, (long long)(INT_MAX / 2));
+    }
     while (true) {
+        if (tid < kSizeBuckets) s_bucket_count[tid] = 0;
+        __syncthreads();
         const int split = s_split;
         long long rows = 0;
         for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
-            const int ns = (a.group_kvb[gi] + split - 1) / split;
+            const int kvb = grp_kvb[gi];
+            const int ns = max(1, (kvb + split - 1) / split);
             if (ns > 1) {
-                const int r = a.group_req[gi];
+                const int r = grp_req[gi];
                 rows += (long long)ns * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
+                atomicAdd(&s_bucket_count[0], (ns - 1) * Hkv);
             }
+            atomicAdd(&s_bucket_count[size_bucket(kvb - (ns - 1) * split, split)], Hkv);
         }
         rows = block_sum<long long>(rows, s_ll);
         if (rows <= a.part_rows_cap) break;
         if (tid == 0) s_split = split > INT_MAX / 4 ? INT_MAX / 2 : split * 2;
-        __syncthreads();
     }
     const int split = s_split;
-
-    // 4. count items per size bucket.
-    for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
-        const int kvb = a.group_kvb[gi];
-        const int ns = max(1, (kvb + split - 1) / split);
-        const int last = kvb - (ns - 1) * split;
-        if (ns > 1) atomicAdd(&s_bucket_count[0], (ns - 1) * Hkv);
-        atomicAdd(&s_bucket_count[size_bucket(last, split)], Hkv);
-    }
-    __syncthreads();
     if (tid == 0) {
-        int acc = 0;
+        int acc = 0, cacc = 0;
         for (int b = 0; b < kSizeBuckets; ++b) {
             s_bucket_base[b] = acc;
             acc += s_bucket_count[b];
+            s_cbucket_base[b] = cacc;
+            cacc += s_cbucket_count[b];
         }
         a.header->n_items = (int)min((long long)acc, a.items_cap);
         if (acc > a.items_cap) atomicOr(status, PKV_DEV_OVERFLOW);
+        a.header->n_chunk_items = cacc;
+        a.header->split_blocks = split;
+        a.header->n_groups = n_groups;
     }
     __syncthreads();
 
-    // 5. partial-row bases (chunked scan over groups) and the items.
+    // 4. partial-row bases (chunked scan over groups) and the decode items.
     int row_carry = 0;
     for (int base = 0; base < n_groups; base += kPlanThreads) {
         const int gi = base + tid;
         int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
         if (gi < n_groups) {
-            r = a.group_req[gi];
+            r = grp_req[gi];
             mt = gi - req_g[r];
-            kvb = a.group_kvb[gi];
+            kvb = grp_kvb[gi];
             ns = max(1, (kvb + split - 1) / split);
             nv = tile_rows(req_n[r], g, mt);
         }
@@ -304,59 +329,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         }
         row_carry += tot_rows;
     }
-    if (tid == 0) {
-        a.header->split_blocks = split;
-        a.header->n_groups = n_groups;
-        a.header->n_partial_rows = row_carry;
-    }
+    if (tid == 0) a.header->n_partial_rows = row_carry;
 
-    // 6. chunk items, longest first: 8 buckets of kv_end below the maximum.
-    __syncthreads();
+    // 5. chunk items, longest first.
     for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
         const int r = find_group_request(req_c, R, gi);
         const int mt = gi - req_c[r];
-        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
-        atomicMax(&s_kvmax, req_L[r] - req_n[r] + (int)(last_row / g) + 1);
-    }
-    if (tid < kSizeBuckets) {
-        s_bucket_count[tid] = 0;
-        s_bucket_cursor[tid] = 0;
-    }
-    __syncthreads();
-    const int kvmax = s_kvmax;
-    auto chunk_bucket = [&](int kv_end) {
-        return min(kSizeBuckets - 1, (int)((long long)(kvmax - kv_end) * (kSizeBuckets - 1) / (kvmax + 1)));
-    };
-    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
-        const int r = find_group_request(req_c, R, gi);
-        const int mt = gi - req_c[r];
-        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
-        atomicAdd(&s_bucket_count[chunk_bucket(req_L[r] - req_n[r] + (int)(last_row / g) + 1)], Hkv);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int b = 0; b < kSizeBuckets; ++b) {
-            s_bucket_base[b] = acc;
-            acc += s_bucket_count[b];
-        }
-        a.header->n_chunk_items = acc;
-    }
-    __syncthreads();
-    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
-        const int r = find_group_request(req_c, R, gi);
-        const int mt = gi - req_c[r];
-        const int n = req_n[r], L = req_L[r];
+        const int n = req_n[r];
         const long long rows = (long long)n * g;
-        const long long last_row = min(rows - 1, (long long)mt * kChunkRows + kChunkRows - 1);
-        const int kv_end = L - n + (int)(last_row / g) + 1;
+        const int kv_end = chunk_kv_end(r, mt);
         const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
         const int b = chunk_bucket(kv_end);
         for (int h = 0; h < Hkv; ++h) {
-            const int idx = s_bucket_base[b] + atomicAdd(&s_bucket_cursor[b], 1);
+            const int idx = s_cbucket_base[b] + atomicAdd(&s_cbucket_cursor[b], 1);
             ChunkItem c;
             c.a = make_int4(r, mt, h, kv_end);
-            c.b = make_int4(req_q0[r], n, L, nv);
+            c.b = make_int4(req_q0[r], n, req_L[r], nv);
             a.chunk_items[idx] = c;
         }
     }
@@ -433,7 +421,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = &a.header->status;
-    const int n_items = a.header->n_items;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -448,6 +435,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         mbar_fence_init();
     }
     __syncthreads();
+    // The prologue above overlaps the previous kernel; the work list it
+    // wrote is read only after this.
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n_items = a.header->n_items;
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -818,7 +810,7 @@ std::mutex g_mu;
 DeviceInfo g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kPlanSmemBytes = kReqCacheArrays * (kPlanSmemReqs + 1) * 4;
+constexpr int kPlanSmemBytes = (kReqCacheArrays * (kPlanSmemReqs + 1) + 2 * kPlanSmemGroups) * 4;
 
 template <int D>
 int decode_occupancy() {
@@ -970,9 +962,14 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.group_kvb = reinterpret_cast<int32_t *>(ws + L.group_kvb);
     pa.tile_counter = reinterpret_cast<int32_t *>(ws + L.tile_counter);
     pa.items = reinterpret_cast<WorkItem *>(ws + L.items);
-    const int plan_smem = num_reqs <= kPlanSmemReqs ? kReqCacheArrays * (num_reqs + 1) * 4 : 0;
+    int plan_smem = 0;
+    if (num_reqs <= kPlanSmemReqs) {
+        plan_smem = kReqCacheArrays * (num_reqs + 1) * 4;
+        if (L.groups_cap <= kPlanSmemGroups) plan_smem += 2 * (int)L.groups_cap * 4;
+    }
     record(events, 0, st);
-    plan_kernel<<<1, kPlanThreads, plan_smem, st>>>(pa);
+    cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), plan_smem, st, pa);
+    if (err != cudaSuccess) return PKV_E_CUDA;
     record(events, 1, st);
 
     DecodeArgs da;
@@ -1003,13 +1000,15 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.items = pa.chunk_items;
         ca.header = header;
         ca.out = static_cast<__nv_bfloat16 *>(out);
-        chunk_launch(D, di->sm_count, kv_map, q_map, ca, st);
+        if (chunk_launch(D, di->sm_count, kv_map, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     }
     record(events, 2, st);
-    if (D == 128) decode_kernel<128><<<ctas, kDecodeThreads, DecodeSmem<128>::kAlloc, st>>>(kv_map, da);
-    else decode_kernel<64><<<ctas, kDecodeThreads, DecodeSmem<64>::kAlloc, st>>>(kv_map, da);
+    if (D == 128)
+        err = launch_pdl(decode_kernel<128>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<128>::kAlloc, st, kv_map, da);
+    else
+        err = launch_pdl(decode_kernel<64>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<64>::kAlloc, st, kv_map, da);
     record(events, 3, st);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    return err == cudaSuccess && cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 }  // namespace

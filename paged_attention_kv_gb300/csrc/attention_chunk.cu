@@ -27,6 +27,7 @@
 #include "attention_plan.cuh"
 #include "pagedkv.h"
 #include "pkv_device.cuh"
+#include "pkv_host.h"
 
 namespace pkv {
 namespace {
@@ -73,7 +74,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     volatile int *abort = &s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = &a.header->status;
-    const int n_items = a.header->n_chunk_items;
     const int g = a.group;
 
     if (threadIdx.x == 0) {
@@ -98,6 +98,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tm = *tmem_slot;
+    // The prologue above overlaps the previous kernel; the work list it
+    // wrote is read only after this.
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n_items = a.header->n_chunk_items;
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
@@ -388,12 +393,13 @@ int chunk_configure() {
     return PKV_OK;
 }
 
-void chunk_launch(int head_size, int grid, const CUtensorMap &kv_map, const CUtensorMap &q_map, const ChunkArgs &args,
-                  cudaStream_t stream) {
+cudaError_t chunk_launch(int head_size, int grid, const CUtensorMap &kv_map, const CUtensorMap &q_map,
+                         const ChunkArgs &args, cudaStream_t stream) {
     if (head_size == 128)
-        chunk_kernel<128><<<grid, kChunkThreads, ChunkSmem<128>::kAlloc, stream>>>(kv_map, q_map, args);
-    else
-        chunk_kernel<64><<<grid, kChunkThreads, ChunkSmem<64>::kAlloc, stream>>>(kv_map, q_map, args);
+        return launch_pdl(chunk_kernel<128>, dim3(grid), dim3(kChunkThreads), ChunkSmem<128>::kAlloc, stream, kv_map,
+                          q_map, args);
+    return launch_pdl(chunk_kernel<64>, dim3(grid), dim3(kChunkThreads), ChunkSmem<64>::kAlloc, stream, kv_map, q_map,
+                      args);
 }
 
 }  // namespace pkv

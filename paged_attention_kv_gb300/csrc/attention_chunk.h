@@ -27,7 +27,7 @@ struct ChunkArgs {
 
 int chunk_smem_bytes(int head_size);
 int chunk_configure();  // kernel attributes; once per device
-void chunk_launch(int head_size, int grid, const CUtensorMap &kv_map, const CUtensorMap &q_map, const ChunkArgs &args,
-                  cudaStream_t stream);
+cudaError_t chunk_launch(int head_size, int grid, const CUtensorMap &kv_map, const CUtensorMap &q_map,
+                         const ChunkArgs &args, cudaStream_t stream);
 
 }  // namespace pkv

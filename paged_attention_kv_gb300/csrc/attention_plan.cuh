@@ -37,7 +37,8 @@ constexpr int kMinSplitBlocks = 4;   // at least one block per consumer warp
 // items per CTA and >= 256 KiB of K+V per item).
 constexpr int kMinItemBytes = PKV_MIN_ITEM_KB << 10;  // at least this much K+V per item
 constexpr int kItemsPerCta = PKV_ITEMS_PER_CTA;      // items per persistent CTA
-constexpr int kPlanSmemReqs = 4096;  // per-request tables kept in shared memory up to this many requests
+constexpr int kPlanSmemReqs = 4096;    // per-request tables kept in shared memory up to this many requests
+constexpr int kPlanSmemGroups = 8192;  // per-group tables likewise, up to this many decode groups
 constexpr int kSizeBuckets = 9;      // 0 = full-size split, 1..8 = shorter, longest first
 
 // Chunk tiles (tcgen05 path): requests with at least kChunkRows query rows

@@ -101,6 +101,18 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialisation) start its prologue while this one runs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the previous kernel on the stream has completed and its
+// memory is visible (returns at once for a normally launched kernel). Every
+// kernel calls it before it touches global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- named barrier --------------------------------------------------------
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {

@@ -1,8 +1,11 @@
 // Host-side helpers shared by the C-ABI translation units.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "pagedkv.h"
 
@@ -25,6 +28,26 @@ inline int check_cache_desc(const pkv_cache_desc &d, bool attention) {
     if (d.num_blocks > INT32_MAX / PKV_BLOCK_SIZE) return PKV_E_DIMS;
     if (d.num_kv_heads > 4096 || d.head_size > 4096) return PKV_E_DIMS;
     return PKV_OK;
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream is still running; it calls pdl_wait()
+// before touching global memory, so it still sees all of that kernel's
+// writes, and it cannot complete before its predecessor has.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace pkv

@@ -29,6 +29,8 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int
                                     const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ qsl,
                                     int num_tokens, int num_blocks, int32_t *__restrict__ slot_mapping,
                                     int32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t == 0 && (__ldg(qsl) != 0 || __ldg(qsl + num_reqs) != num_tokens)) raise_status(status, PKV_DEV_BAD_QSL);
     if (t >= num_tokens) return;
@@ -59,6 +61,8 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__rest
                                 const int32_t *__restrict__ slot_mapping, long long num_tokens,
                                 uint4 *__restrict__ kv_cache, long long num_slots, int num_kv_heads,
                                 int chunks_per_row, int32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long per_kv = (long long)num_kv_heads * chunks_per_row;
     const long long total = num_tokens * 2 * per_kv;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -102,10 +106,10 @@ extern "C" PKV_API int paged_slot_mapping(const int32_t *block_table, int32_t nu
         return PKV_E_ALIGN;
     const int threads = 256;
     const int blocks = (num_tokens + threads - 1) / threads;
-    slot_mapping_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        block_table, num_reqs, max_blocks_per_req, seq_lens, query_start_loc, num_tokens, num_blocks, slot_mapping,
-        status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    const cudaError_t err = launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0,
+                                       static_cast<cudaStream_t>(stream), block_table, num_reqs, max_blocks_per_req,
+                                       seq_lens, query_start_loc, num_tokens, num_blocks, slot_mapping, status);
+    return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
@@ -124,9 +128,10 @@ extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_
     const int threads = 256;
     const long long want = (total + threads - 1) / threads;
     const int blocks = (int)(want < (1 << 20) ? want : (1 << 20));
-    kv_write_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
-        static_cast<uint4 *>(kv_cache), (long long)desc->num_blocks * PKV_BLOCK_SIZE, desc->num_kv_heads,
+    const cudaError_t err = launch_pdl(
+        kv_write_kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream),
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, (long long)num_tokens,
+        static_cast<uint4 *>(kv_cache), (long long)desc->num_blocks * PKV_BLOCK_SIZE, (int)desc->num_kv_heads,
         chunks_per_row, status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
