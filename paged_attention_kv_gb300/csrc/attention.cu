@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.header->status = 0;
         a.header->next_item = 0;
         a.header->next_chunk_item = 0;
+        a.header->diag = 0;
         s_kvmax = 0;
     }
     if (tid < kSizeBuckets) {
@@ -543,12 +544,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         // memory are still in flight: wait (bounded) for the last issue of
         // every stage.
         if (!ok && lane == 0) {
-            for (uint32_t x = e > (uint32_t)S::kStages ? e - S::kStages : 0; x < e; ++x) {
-                const uint32_t stage = x % S::kStages, parity = (x / S::kStages) & 1;
-                const unsigned long long t0 = global_timer_ns();
-                while (!mbar_try_wait(&full[stage], parity) && global_timer_ns() - t0 < kWaitTimeoutNs) {
-                }
-            }
+            for (uint32_t x = e > (uint32_t)S::kStages ? e - S::kStages : 0; x < e; ++x)
+                mbar_drain(&full[x % S::kStages], (x / S::kStages) & 1, status, &a.header->diag, 0x1);
         }
         return;
     }

@@ -36,6 +36,23 @@ constexpr int kChunkThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8
 
+// mbarrier slots: the Q tile handoff, the K/V ring and S buffers (two each,
+// by tile parity), P ready, PV done, and the final drain.
+enum ChunkBar {
+    kBarQFull = 0,
+    kBarQEmpty,
+    kBarQTaken,
+    kBarKFull,                    // [2]
+    kBarVFull = kBarKFull + 2,    // [2]
+    kBarKvEmpty = kBarVFull + 2,  // [2]
+    kBarSFull = kBarKvEmpty + 2,  // [2]
+    kBarSFree = kBarSFull + 2,    // [2]
+    kBarPFull = kBarSFree + 2,
+    kBarODone,
+    kBarDrain,
+    kNumBars
+};
+
 struct ChunkDesc {
     int item, r, mt, h, kv_end, q0, n, L, nv, nt, pad[6];
 };
@@ -50,8 +67,7 @@ struct ChunkSmem {
     static constexpr int kOffP = kOffV + 2 * kTile; // 128 rows x 128 keys bf16, two 64-key halves
     static constexpr int kOffDesc = kOffP + 2 * kHalf;
     static constexpr int kOffBar = kOffDesc + (int)sizeof(ChunkDesc);
-    // q_full, q_empty, q_taken, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, drain
-    static constexpr int kBars = 16;
+    static constexpr int kBars = kNumBars;
     static constexpr int kOffTmem = kOffBar + kBars * 8;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -66,14 +82,16 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     __shared__ int s_abort;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
-    uint64_t *q_full = bar + 0, *q_empty = bar + 1, *q_taken = bar + 2;
-    uint64_t *k_full = bar + 3, *v_full = bar + 5, *kv_empty = bar + 7;
-    uint64_t *s_full = bar + 9, *s_free = bar + 11, *p_full = bar + 13, *o_done = bar + 14, *drain = bar + 15;
+    uint64_t *q_full = bar + kBarQFull, *q_empty = bar + kBarQEmpty, *q_taken = bar + kBarQTaken;
+    uint64_t *k_full = bar + kBarKFull, *v_full = bar + kBarVFull, *kv_empty = bar + kBarKvEmpty;
+    uint64_t *s_full = bar + kBarSFull, *s_free = bar + kBarSFree, *p_full = bar + kBarPFull;
+    uint64_t *o_done = bar + kBarODone, *drain = bar + kBarDrain;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffTmem);
     ChunkDesc *desc = reinterpret_cast<ChunkDesc *>(smem + S::kOffDesc);
     volatile int *abort = &s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = &a.header->status;
+    int32_t *diag = &a.header->diag;
     const int g = a.group;
 
     if (threadIdx.x == 0) {
@@ -178,10 +196,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
         if (!ok && lane == 0) {
             // let copies already issued land before the CTA can leave
             for (uint32_t x = jt > 2 ? jt - 2 : 0; x < jt; ++x) {
-                const unsigned long long t0 = global_timer_ns();
-                while (!(mbar_try_wait(&k_full[x & 1], (x >> 1) & 1) && mbar_try_wait(&v_full[x & 1], (x >> 1) & 1)) &&
-                       global_timer_ns() - t0 < kWaitTimeoutNs) {
-                }
+                mbar_drain(&k_full[x & 1], (x >> 1) & 1, status, diag, 0x2);
+                mbar_drain(&v_full[x & 1], (x >> 1) & 1, status, diag, 0x2);
             }
         }
     } else if (warp == 1) {
@@ -237,9 +253,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
             }
             // make sure no MMA is still writing TMEM before it is freed
             umma_commit(drain);
-            const unsigned long long t0 = global_timer_ns();
-            while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < kWaitTimeoutNs) {
-            }
+            mbar_drain(drain, 0, status, diag, 0x4);
         }
         __syncwarp();
     } else {

@@ -55,7 +55,8 @@ struct WsHeader {
     int32_t next_item;     // dynamic scheduling counter
     int32_t n_chunk_items;
     int32_t next_chunk_item;
-    int32_t pad[56];
+    int32_t diag;          // bits naming the pipeline waits that timed out (PKV_DEV_TIMEOUT)
+    int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 

@@ -79,6 +79,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
+// mbar_wait that, when it is the one that times out, also ORs `site` into
+// *diag so the waiting point can be identified afterwards.
+__device__ __forceinline__ bool mbar_wait_at(uint64_t *bar, uint32_t parity, int32_t *status, volatile int *abort,
+                                             int32_t *diag, int32_t site) {
+    const int was = *abort;
+    if (mbar_wait(bar, parity, status, abort)) return true;
+    if (!was && diag && *abort) {
+        // abort was clear when we started; it is set now either by this wait's
+        // timeout or by another thread's; record the site either way
+        atomicOr(diag, site);
+    }
+    return false;
+}
+
+// Bounded poll of `bar` used when leaving a CTA after a failure or to drain
+// asynchronous work; a timeout is reported like any other.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, int32_t *status, int32_t *diag,
+                                           int32_t site) {
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            raise_status(status, PKV_DEV_TIMEOUT);
+            if (diag) atomicOr(diag, site);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
