@@ -58,6 +58,10 @@ def parse_args():
     p.add_argument("--workload", default="llama8b")
     p.add_argument("--skip-cpu-baseline", action="store_true", help="leave out the oracle CPU baseline")
     p.add_argument("--skip-e2e", action="store_true", help="leave out the end-to-end (host buffers) loop")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the step from a captured CUDA graph in the timed loop")
+    p.add_argument("--op", choices=("step", "kv_transfer"), default="step",
+                   help="kv_transfer: time block gather + scatter of the workload's context blocks")
     return p.parse_args()
 
 
@@ -369,8 +373,12 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     ten = wl.make_tensors(batch, device=dev)
+    if args.op == "kv_transfer":
+        run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world)
+        return
     host = host_copy(ten) if (rank == 0 and world == 1 and not args.skip_cpu_baseline) else None
     buf = pkv.StepBuffers(batch, ten)
+    graph = pkv.StepGraph(buf) if args.graph else None
     stream = torch.cuda.current_stream()
 
     nev = args.steps
@@ -398,7 +406,10 @@ def main():
     wall0 = time.time()
     t_start.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     t_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -451,7 +462,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block tables)",
         "config": {**workload_config(batch), "parallelism": f"{world} independent replicas" if world > 1
-                   else "single GPU"},
+                   else "single GPU", "launch": "CUDA graph replay" if graph is not None else "eager, PDL launches"},
         "roofline": {"bound": "hbm", "kernel": "attention decode_kernel (split-KV)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
@@ -469,6 +480,52 @@ def main():
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world):
+    """Block-granular KV transfer (disaggregated prefill/decode): gather
+    every context block of the batch into a staging buffer, then scatter it
+    back. Bytes: each block read once and written once per direction."""
+    ids = np.unique(np.concatenate([batch.block_table[r, :-(-int(L) // 16)]
+                                    for r, L in enumerate(batch.seq_lens)])).astype(np.int32)
+    ids_d = torch.from_numpy(ids).to(dev)
+    pool = ten["kv_cache"]
+    staging = pkv.paged_kv_gather_blocks(pool, ids_d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        pkv.paged_kv_gather_blocks(pool, ids_d, staging, status)
+        pkv.paged_kv_scatter_blocks(staging, ids_d, pool, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), dist, dev) / args.steps
+    if pkv.pkv_read_status(status):
+        raise RuntimeError("device status bits set")
+    if rank != 0:
+        return
+    nbytes = 2 * 2 * ids.shape[0] * pkv.block_bytes(pool)
+    peaks = measured_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "KV block transfer (gather + scatter) GB/s", "value": world * achieved, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
+        "data": "synthetic", "config": {**workload_config(batch), "blocks": int(ids.shape[0]),
+                                        "bytes_per_step": nbytes},
+        "roofline": {"bound": "hbm", "kernel": "block_copy_kernel", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps}), flush=True)
 
 
 def run_e2e(args, batch, ten, buf, pkv, torch, dev, dist):

@@ -130,6 +130,28 @@ int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, in
                    void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream);
 
 /*
+ * Block-granular KV transfer for disaggregated prefill/decode (page 1,
+ * "Disaggregated P/D": the prefill instance uploads the KV it computed, and
+ * before decoding, start_load_kv loads it and injects it into paged memory;
+ * the transfer may run per layer). One block of one layer is one
+ * contiguous run of block_bytes = 2 * 16 * num_kv_heads * head_size * 2
+ * bytes in the pool layout.
+ *
+ * paged_kv_gather_blocks:  staging[i] = pool block block_ids[i]
+ * paged_kv_scatter_blocks: pool block block_ids[i] = staging[i]
+ *
+ *  staging    bytes [num_ids][block_bytes], device, 16-byte aligned
+ *  block_ids  int32 [num_ids], device. An id outside [0, num_blocks) is
+ *             skipped (its staging slot, or nothing, is left as it was) and
+ *             raises PKV_DEV_BAD_BLOCK. Scatter ids must be distinct.
+ *  status     optional device int32, PKV_DEV_* bits OR-ed in.
+ */
+int paged_kv_gather_blocks(const void *kv_cache, const pkv_cache_desc *desc, const int32_t *block_ids,
+                           int32_t num_ids, void *staging, int32_t *status, void *stream);
+int paged_kv_scatter_blocks(const void *staging, const int32_t *block_ids, int32_t num_ids, void *kv_cache,
+                            const pkv_cache_desc *desc, int32_t *status, void *stream);
+
+/*
  * Workspace bytes paged_attention needs for batches of at most
  * max_num_reqs requests and max_num_tokens new tokens on the current
  * device. A smaller workspace (down to the size for max_num_reqs and

@@ -51,6 +51,12 @@ def _load():
         lib.orc_kv_write.restype = ctypes.c_int
         lib.orc_kv_write.argtypes = [u16p, u16p, i32p, ctypes.c_int, u16p,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.orc_kv_gather_blocks.restype = ctypes.c_int
+        lib.orc_kv_gather_blocks.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             i32p, ctypes.c_int, u16p]
+        lib.orc_kv_scatter_blocks.restype = ctypes.c_int
+        lib.orc_kv_scatter_blocks.argtypes = [u16p, i32p, ctypes.c_int, u16p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int]
         lib.orc_paged_attention_rows.restype = ctypes.c_int
         lib.orc_paged_attention_rows.argtypes = [
             u16p, ctypes.c_int, ctypes.c_int,
@@ -116,6 +122,30 @@ def kv_write(kv_cache: np.ndarray, k, v, slots) -> None:
     rc = _load().orc_kv_write(_ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16), _ptr(s, ctypes.c_int32),
                               s.shape[0], _ptr(kv_cache, ctypes.c_uint16), nb, bs, hkv, d)
     _check(rc, "kv_write")
+
+
+def kv_gather_blocks(kv_cache: np.ndarray, block_ids) -> np.ndarray:
+    """uint16 [n][2][Hkv][B][D]: copies of the pool blocks block_ids[i]."""
+    assert kv_cache.dtype == np.uint16 and kv_cache.flags.c_contiguous and kv_cache.ndim == 5
+    nb, _, hkv, bs, d = kv_cache.shape
+    ids = _c(block_ids, np.int32)
+    out = np.zeros((ids.shape[0], 2, hkv, bs, d), dtype=np.uint16)
+    rc = _load().orc_kv_gather_blocks(_ptr(kv_cache, ctypes.c_uint16), nb, bs, hkv, d, _ptr(ids, ctypes.c_int32),
+                                      ids.shape[0], _ptr(out, ctypes.c_uint16))
+    _check(rc, "kv_gather_blocks")
+    return out
+
+
+def kv_scatter_blocks(staging, block_ids, kv_cache: np.ndarray) -> None:
+    """Writes staging[i] into pool block block_ids[i] (in place)."""
+    assert kv_cache.dtype == np.uint16 and kv_cache.flags.c_contiguous and kv_cache.ndim == 5
+    nb, _, hkv, bs, d = kv_cache.shape
+    ids = _c(block_ids, np.int32)
+    st = _c(staging, np.uint16)
+    assert st.size == ids.shape[0] * 2 * hkv * bs * d
+    rc = _load().orc_kv_scatter_blocks(_ptr(st, ctypes.c_uint16), _ptr(ids, ctypes.c_int32), ids.shape[0],
+                                       _ptr(kv_cache, ctypes.c_uint16), nb, bs, hkv, d)
+    _check(rc, "kv_scatter_blocks")
 
 
 def paged_attention(q, kv_cache: np.ndarray, block_table, seq_lens, query_start_loc, scale: float,

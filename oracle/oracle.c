@@ -139,6 +139,46 @@ int orc_kv_write(const uint16_t *k, const uint16_t *v, const int32_t *slot_mappi
     return ORC_OK;
 }
 
+/* Block-granular KV transfer for disaggregated prefill/decode (page 1,
+ * "Disaggregated P/D": the decode instance loads the KV the prefill instance
+ * computed and injects it into paged memory). staging is [num_ids][block]
+ * with block = 2 * B * Hkv * D elements, the whole unit of one physical
+ * block; gather copies pool blocks out, scatter copies them in. An id
+ * outside the pool is an error. */
+int orc_kv_gather_blocks(const uint16_t *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                         int head_size, const int32_t *block_ids, int num_ids, uint16_t *staging) {
+    const int64_t per_block = (int64_t)2 * block_size * num_kv_heads * head_size;
+    for (int i = 0; i < num_ids; ++i) {
+        if (block_ids[i] < 0 || block_ids[i] >= num_blocks) return ORC_E_BLOCK;
+        for (int kv = 0; kv < 2; ++kv)
+            for (int h = 0; h < num_kv_heads; ++h)
+                for (int row = 0; row < block_size; ++row) {
+                    const uint16_t *src = kv_cache + cache_row(block_ids[i], kv, h, row, num_kv_heads, block_size, head_size);
+                    uint16_t *dst = staging + (int64_t)i * per_block +
+                                    (((int64_t)kv * num_kv_heads + h) * block_size + row) * head_size;
+                    for (int d = 0; d < head_size; ++d) dst[d] = src[d];
+                }
+    }
+    return ORC_OK;
+}
+
+int orc_kv_scatter_blocks(const uint16_t *staging, const int32_t *block_ids, int num_ids, uint16_t *kv_cache,
+                          int num_blocks, int block_size, int num_kv_heads, int head_size) {
+    const int64_t per_block = (int64_t)2 * block_size * num_kv_heads * head_size;
+    for (int i = 0; i < num_ids; ++i) {
+        if (block_ids[i] < 0 || block_ids[i] >= num_blocks) return ORC_E_BLOCK;
+        for (int kv = 0; kv < 2; ++kv)
+            for (int h = 0; h < num_kv_heads; ++h)
+                for (int row = 0; row < block_size; ++row) {
+                    uint16_t *dst = kv_cache + cache_row(block_ids[i], kv, h, row, num_kv_heads, block_size, head_size);
+                    const uint16_t *src = staging + (int64_t)i * per_block +
+                                          (((int64_t)kv * num_kv_heads + h) * block_size + row) * head_size;
+                    for (int d = 0; d < head_size; ++d) dst[d] = src[d];
+                }
+    }
+    return ORC_OK;
+}
+
 typedef struct {
     const uint16_t *q;
     const uint16_t *kv_cache;

@@ -37,7 +37,8 @@ PKV_DEV_BAD_SLOT = 0x8
 PKV_DEV_TIMEOUT = 0x10
 PKV_DEV_OVERFLOW = 0x20
 
-EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_attention_workspace_bytes",
+EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_gather_blocks",
+            "paged_kv_scatter_blocks", "paged_attention_workspace_bytes",
             "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
             "paged_attention_static", "pkv_read_status", "pkv_status_string")
 
@@ -62,6 +63,8 @@ def _load():
     lib.pkv_kv_cache_bytes.argtypes = [desc_p, ctypes.POINTER(sz)]
     lib.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
     lib.paged_kv_write.argtypes = [vp, vp, vp, i32, vp, desc_p, vp, vp]
+    lib.paged_kv_gather_blocks.argtypes = [vp, desc_p, vp, i32, vp, vp, vp]
+    lib.paged_kv_scatter_blocks.argtypes = [vp, vp, i32, vp, desc_p, vp, vp]
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
     lib.paged_attention_min_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
     lib.paged_attention.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, sz, vp]
@@ -157,6 +160,40 @@ def paged_kv_write(k, v, slot_mapping, kv_cache, status=None, stream=None) -> No
         raise ValueError("slot_mapping is shorter than k")
     _check(LIB.paged_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(kv_cache), ctypes.byref(desc),
                               _ptr(status), _stream(stream)), "paged_kv_write")
+
+
+def block_bytes(kv_cache: torch.Tensor) -> int:
+    d = cache_desc(kv_cache)
+    return 2 * d.block_size * d.num_kv_heads * d.head_size * 2
+
+
+def paged_kv_gather_blocks(kv_cache, block_ids, staging=None, status=None, stream=None) -> torch.Tensor:
+    """staging[i] = pool block block_ids[i]; staging is uint8 [n][block_bytes]."""
+    _want(kv_cache, torch.bfloat16, 5, "kv_cache")
+    _want(block_ids, torch.int32, 1, "block_ids")
+    n = block_ids.shape[0]
+    if staging is None:
+        staging = torch.empty((n, block_bytes(kv_cache)), dtype=torch.uint8, device=kv_cache.device)
+    _want(staging, torch.uint8, 2, "staging")
+    if staging.shape[0] < n or staging.shape[1] != block_bytes(kv_cache):
+        raise ValueError("staging must be [num_ids][block_bytes] bytes")
+    desc = cache_desc(kv_cache)
+    _check(LIB.paged_kv_gather_blocks(_ptr(kv_cache), ctypes.byref(desc), _ptr(block_ids), n, _ptr(staging),
+                                      _ptr(status), _stream(stream)), "paged_kv_gather_blocks")
+    return staging
+
+
+def paged_kv_scatter_blocks(staging, block_ids, kv_cache, status=None, stream=None) -> None:
+    """pool block block_ids[i] = staging[i]."""
+    _want(kv_cache, torch.bfloat16, 5, "kv_cache")
+    _want(block_ids, torch.int32, 1, "block_ids")
+    _want(staging, torch.uint8, 2, "staging")
+    n = block_ids.shape[0]
+    if staging.shape[0] < n or staging.shape[1] != block_bytes(kv_cache):
+        raise ValueError("staging must be [num_ids][block_bytes] bytes")
+    desc = cache_desc(kv_cache)
+    _check(LIB.paged_kv_scatter_blocks(_ptr(staging), _ptr(block_ids), n, _ptr(kv_cache), ctypes.byref(desc),
+                                       _ptr(status), _stream(stream)), "paged_kv_scatter_blocks")
 
 
 def paged_attention_workspace_bytes(max_num_reqs: int, max_num_tokens: int, num_q_heads: int, num_blocks: int,
@@ -292,6 +329,30 @@ class StepBuffers:
         paged_attention(self.q, self.kv_cache, self.block_table, self.seq_lens, self.query_start_loc,
                         self.batch.scale, self.out, self.workspace, stream)
         return self.out
+
+
+class StepGraph:
+    """One step (slot mapping, KV write, attention) captured into a CUDA
+    graph and replayed: the launches of a step cost one graph launch. The
+    graph keeps the buffers' device addresses, so new inputs of the same
+    shape are copied into ``buffers`` before each replay (the engine loop
+    of the pages captures one graph per warm-up batch size in the same way,
+    page 1, "LLM Engine constructor", KV-cache initialisation)."""
+
+    def __init__(self, buffers: StepBuffers):
+        self.buffers = buffers
+        # first calls set up the device (kernel attributes, entry points)
+        # and must run outside capture
+        buffers.step()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            buffers.step()
+        torch.cuda.synchronize()
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.buffers.out
 
 
 def run_step(batch, tensors: dict, stream=None) -> dict:

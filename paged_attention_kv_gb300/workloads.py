@@ -8,7 +8,7 @@ counts, and block tables made of physical block ids drawn from a shuffled
 pool. It holds none of the attention or KV-write arithmetic; both the CUDA
 path and the CPU oracle read what it produces.
 
-The five workloads:
+The workloads:
 
 ``tiny``       TinyLlama shape (32 q / 4 kv heads, head 64), 2 decode requests
                with contexts 17 and 40, a 64-block pool.
@@ -22,6 +22,11 @@ The five workloads:
 ``prefix``     Llama-3-8B shape, 128 decode requests that share their first 64
                physical blocks (1024 tokens) and own a suffix of s tokens,
                s log-uniform in [64, 31744].
+``specdec``    Llama-3-8B shape, 256 requests verifying 3 draft tokens each:
+               4 new query tokens per request (speculative decoding scores
+               k draft tokens plus one, "Speculative Decoding"; the pages'
+               example sets num_speculative_tokens to 3), contexts uniform
+               in [512, 4096].
 
 Pools are 1.25x the blocks the batch needs (``tiny``: 64 blocks). Q, K, V and
 the pool contents are N(0, 1) drawn in fp32 and rounded to bf16. Blocks that
@@ -51,7 +56,7 @@ class ModelShape:
 TINYLLAMA = ModelShape("TinyLlama-1.1B", 32, 4, 64)
 LLAMA3_8B = ModelShape("Llama-3-8B", 32, 8, 128)
 
-WORKLOADS = ("tiny", "tinyllama", "llama8b", "mixed", "prefix")
+WORKLOADS = ("tiny", "tinyllama", "llama8b", "mixed", "prefix", "specdec")
 
 
 @dataclass
@@ -166,6 +171,12 @@ def make_batch(workload: str, seed_offset: int = 0) -> Batch:
         table, nb = _tables(rng, _ceil_div(seq, bs), shared)
         desc = ("Llama-3-8B shape, 128 decode requests sharing 64 prefix blocks (1024 tokens) "
                 "+ log-uniform suffixes in [64, 31744]")
+    elif workload == "specdec":
+        shape = LLAMA3_8B
+        seq = rng.integers(512, 4096, size=256, endpoint=True)
+        qlen = np.full(256, 4, dtype=np.int64)
+        table, nb = _tables(rng, _ceil_div(seq, bs), 0)
+        desc = "Llama-3-8B shape, 256 requests verifying 3 draft tokens (4 query tokens each), contexts U[512,4096]"
     else:
         raise ValueError(f"unknown workload {workload!r}; expected one of {WORKLOADS}")
     return Batch(workload=workload, shape=shape, seq_lens=seq.astype(np.int32),

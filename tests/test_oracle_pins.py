@@ -332,3 +332,34 @@ def test_oracle_rejects_bad_batches():
     with pytest.raises(oracle.OracleError):
         oracle.kv_write(np.zeros((2, 2, 1, B, 8), np.uint16), np.zeros((1, 1, 8), np.uint16),
                         np.zeros((1, 1, 8), np.uint16), np.array([40], np.int32))
+
+
+# --- block transfer (disaggregated prefill/decode) ---------------------------
+
+def test_block_gather_copies_the_formula_sized_contiguous_unit():
+    """Page 1 "Disaggregated P/D": KV moves into / out of paged memory by
+    block. A gathered block is exactly the contiguous byte range
+    [b * block_bytes, (b + 1) * block_bytes) of the pool (page 2 formula)."""
+    rng = np.random.default_rng(60)
+    hkv, d = 2, 16
+    cache = _bf16(rng.standard_normal((9, 2, hkv, B, d)))
+    ids = np.array([7, 0, 3, 7], np.int32)
+    got = oracle.kv_gather_blocks(cache, ids)
+    nbytes = oracle.block_bytes(B, hkv, d, 2)
+    raw = cache.view(np.uint8).reshape(-1)
+    for i, b in enumerate(ids):
+        assert np.array_equal(got[i].view(np.uint8).reshape(-1), raw[b * nbytes:(b + 1) * nbytes])
+
+
+def test_block_scatter_then_gather_round_trips_and_touches_only_targets():
+    rng = np.random.default_rng(61)
+    hkv, d = 2, 8
+    cache = _bf16(rng.standard_normal((6, 2, hkv, B, d)))
+    before = cache.copy()
+    staged = _bf16(rng.standard_normal((2, 2, hkv, B, d)))
+    oracle.kv_scatter_blocks(staged, np.array([4, 1], np.int32), cache)
+    assert np.array_equal(oracle.kv_gather_blocks(cache, np.array([4, 1], np.int32)), staged)
+    untouched = [0, 2, 3, 5]
+    assert np.array_equal(cache[untouched], before[untouched])
+    with pytest.raises(oracle.OracleError):
+        oracle.kv_gather_blocks(cache, np.array([6], np.int32))

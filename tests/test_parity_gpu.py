@@ -252,3 +252,48 @@ def test_back_to_back_steps_finish_promptly_with_clean_status(workload):
     assert pkv.pkv_read_status(buf.status) == 0
     assert pkv.pkv_read_status(buf.workspace) == 0
     assert torch.equal(first.view(torch.int16), buf.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("workload", ["tinyllama", "mixed"])
+def test_graph_replay_matches_eager_step(workload):
+    """A step captured into a CUDA graph and replayed gives the same bits as
+    the eager step, with clean status words."""
+    batch = wl.make_batch(workload)
+    ten = device_tensors(batch)
+    eager = pkv.StepBuffers(batch, {k: v.clone() for k, v in ten.items()})
+    ref = eager.step().clone()
+    g = pkv.StepGraph(pkv.StepBuffers(batch, ten))
+    for _ in range(3):
+        out = g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert pkv.pkv_read_status(g.buffers.status) == 0
+    assert pkv.pkv_read_status(g.buffers.workspace) == 0
+
+
+@pytest.mark.parametrize("shape", [TINY, LLAMA], ids=["d64", "d128"])
+def test_kv_block_gather_scatter_bit_exact(shape):
+    """Block-granular transfer for disaggregated prefill/decode: gather and
+    scatter match the oracle byte for byte; a bad id is skipped and flagged."""
+    batch = _custom(shape, [300, 1000, 77], [1, 1, 1], 300)
+    ten = device_tensors(batch, generate_on="cpu")
+    pool = ten["kv_cache"]
+    host_pool = wl.bf16_bits(pool).copy()
+    rng = np.random.default_rng(301)
+    ids = rng.choice(batch.num_blocks, size=37, replace=False).astype(np.int32)
+    staged = pkv.paged_kv_gather_blocks(pool, torch.from_numpy(ids).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.kv_gather_blocks(host_pool, ids)
+    assert np.array_equal(staged.cpu().numpy().view(np.uint16).reshape(ref.shape), ref)
+    # inject fresh blocks into other slots
+    dst = rng.choice(np.setdiff1d(np.arange(batch.num_blocks), ids), size=37, replace=False).astype(np.int32)
+    fresh = wl.bf16_bits(torch.randn(37, *pool.shape[1:]).to(torch.bfloat16))
+    pkv.paged_kv_scatter_blocks(torch.from_numpy(fresh.view(np.uint8).reshape(37, -1)).cuda(),
+                                torch.from_numpy(dst).cuda(), pool)
+    torch.cuda.synchronize()
+    oracle.kv_scatter_blocks(fresh, dst, host_pool)
+    assert np.array_equal(wl.bf16_bits(pool), host_pool)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = torch.tensor([0, batch.num_blocks + 3, -1], dtype=torch.int32, device="cuda")
+    pkv.paged_kv_gather_blocks(pool, bad, status=status)
+    assert pkv.pkv_read_status(status) & pkv.PKV_DEV_BAD_BLOCK

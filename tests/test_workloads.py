@@ -50,6 +50,8 @@ def test_workload_shapes():
     assert (px.block_table[:, :64] == px.block_table[0, :64]).all()
     s = px.seq_lens - 1024
     assert s.min() >= 64 and s.max() <= 31744 and px.seq_lens.max() <= 32768
+    sd = wl.make_batch("specdec")
+    assert sd.num_reqs == 256 and (sd.query_lens == 4).all() and sd.num_tokens == 1024
 
 
 def test_seeds_are_reproducible_and_distinct():
