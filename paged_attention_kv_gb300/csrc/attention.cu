@@ -56,6 +56,7 @@ struct PlanArgs {
     int32_t *group_kvb;
     int32_t *tile_counter;
     WorkItem *items;
+    GroupRec *group_rec;
     ChunkItem *chunk_items;
 };
 
@@ -123,6 +124,19 @@ __device__ __forceinline__ int size_bucket(int size, int split) {
     return kSizeBuckets - 1 - min(kSizeBuckets - 2, (int)((long long)size * (kSizeBuckets - 1) / split));
 }
 
+// All 32 lanes call this together; each lane with key >= 0 claims `per`
+// consecutive slots of counters[key] and gets the first one. Lanes of the
+// warp with the same key share one shared-memory atomic.
+__device__ __forceinline__ int warp_claim(int key, int per, int *counters) {
+    const int lane = threadIdx.x & 31;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (lane == leader && key >= 0) base = atomicAdd(&counters[key], per * __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return base + per * __popc(peers & ((1u << lane) - 1u));
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     // Dynamic shared memory: the per-request tables when the batch has at
     // most kPlanSmemReqs requests, then the per-group tables when there are
@@ -131,7 +145,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __shared__ long long s_ll[32];
     __shared__ unsigned long long s_ull[32];
     __shared__ int s_i[32];
-    __shared__ int s_split, s_kvmax;
+    __shared__ int s_split, s_kvmax, s_full_total, s_full_count;
+    __shared__ int4 s_place[kPlanThreads];  // per group of a chunk: first full-split item, first tail item, splits
     __shared__ int s_bucket_count[kSizeBuckets], s_bucket_base[kSizeBuckets], s_bucket_cursor[kSizeBuckets];
     __shared__ int s_cbucket_count[kSizeBuckets], s_cbucket_base[kSizeBuckets], s_cbucket_cursor[kSizeBuckets];
     pdl_launch_dependents();
@@ -240,9 +255,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     auto chunk_bucket = [&](int kv_end) {  // longest first
         return min(kSizeBuckets - 1, (int)((long long)(kvmax - kv_end) * (kSizeBuckets - 1) / (kvmax + 1)));
     };
-    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
-        const int r = find_group_request(req_c, R, gi);
-        atomicAdd(&s_cbucket_count[chunk_bucket(chunk_kv_end(r, gi - req_c[r]))], Hkv);
+    for (int base = 0; base < n_cgroups; base += kPlanThreads) {
+        const int gi = base + tid;
+        int key = -1;
+        if (gi < n_cgroups) {
+            const int r = find_group_request(req_c, R, gi);
+            key = chunk_bucket(chunk_kv_end(r, gi - req_c[r]));
+        }
+        warp_claim(key, Hkv, s_cbucket_count);
     }
     work = block_sum<long long>(work, s_ll);  // (its barriers also publish the group tables)
 
@@ -257,18 +277,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     }
     while (true) {
         if (tid < kSizeBuckets) s_bucket_count[tid] = 0;
+        if (tid == 0) s_full_count = 0;
         __syncthreads();
         const int split = s_split;
         long long rows = 0;
-        for (int gi = tid; gi < n_groups; gi += kPlanThreads) {
-            const int kvb = grp_kvb[gi];
-            const int ns = max(1, (kvb + split - 1) / split);
-            if (ns > 1) {
-                const int r = grp_req[gi];
-                rows += (long long)ns * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
-                atomicAdd(&s_bucket_count[0], (ns - 1) * Hkv);
+        for (int base = 0; base < n_groups; base += kPlanThreads) {
+            const int gi = base + tid;
+            int full = 0, tail_key = -1;
+            if (gi < n_groups) {
+                const int kvb = grp_kvb[gi];
+                const int ns = max(1, (kvb + split - 1) / split);
+                if (ns > 1) {
+                    const int r = grp_req[gi];
+                    rows += (long long)ns * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
+                    full = (ns - 1) * Hkv;
+                }
+                tail_key = size_bucket(kvb - (ns - 1) * split, split);
             }
-            atomicAdd(&s_bucket_count[size_bucket(kvb - (ns - 1) * split, split)], Hkv);
+            const int full_warp = __reduce_add_sync(0xffffffffu, full);
+            if ((tid & 31) == 0 && full_warp) {
+                atomicAdd(&s_bucket_count[0], full_warp);
+                atomicAdd(&s_full_count, full_warp);
+            }
+            warp_claim(tail_key, Hkv, s_bucket_count);
         }
         rows = block_sum<long long>(rows, s_ll);
         if (rows <= a.part_rows_cap) break;
@@ -276,6 +307,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     }
     const int split = s_split;
     if (tid == 0) {
+        s_full_total = s_full_count;
+        s_bucket_cursor[0] = 0;
         int acc = 0, cacc = 0;
         for (int b = 0; b < kSizeBuckets; ++b) {
             s_bucket_base[b] = acc;
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __syncthreads();
 
     // 4. partial-row bases (chunked scan over groups) and the decode items.
-    int row_carry = 0;
+    int row_carry = 0, full_carry = 0;
     for (int base = 0; base < n_groups; base += kPlanThreads) {
         const int gi = base + tid;
         int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
@@ -304,45 +337,65 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             nv = tile_rows(req_n[r], g, mt);
         }
         const int n_rows = (gi < n_groups && ns > 1) ? ns * Hkv * nv : 0;
-        int tot_rows;
-        const int row0 = row_carry + block_exclusive_scan<int>(n_rows, &tot_rows, s_i);
+        const int full_cnt = gi < n_groups ? (ns - 1) * Hkv : 0;
+        // One scan carries the partial rows (low half) and the full-size
+        // split items (high half); both totals are within int range once the
+        // split length fits the capacities.
+        unsigned long long tot;
+        const unsigned long long ex = block_exclusive_scan<unsigned long long>(
+            ((unsigned long long)full_cnt << 32) | (unsigned)n_rows, &tot, s_ull);
+        const int row0 = row_carry + (int)(ex & 0xffffffffu);
+        const int tot_rows = (int)(tot & 0xffffffffu);
+        const int full0 = s_bucket_base[0] + full_carry + (int)(ex >> 32);
+        full_carry += (int)(tot >> 32);
+        const int tail_b = gi < n_groups ? size_bucket(kvb - (ns - 1) * split, split) : -1;
+        // tail items of bucket 0 come after every full-size split
+        const int tail0 = (tail_b > 0 ? s_bucket_base[tail_b] : s_bucket_base[0] + s_full_total) +
+                          warp_claim(tail_b, Hkv, s_bucket_cursor);
         if (gi < n_groups) {
             const int n = req_n[r], L = req_L[r], q0 = req_q0[r];
-            const int kv_end = tile_kv_end(n, L, g, mt);
-            for (int h = 0; h < Hkv; ++h) {
-                const int tile = gi * Hkv + h;
-                const int prow0 = ns > 1 ? row0 + h * ns * nv : -1;
-                if (ns > 1) a.tile_counter[tile] = 0;
-                for (int s = 0; s < ns; ++s) {
-                    const int kb0 = s * split;
-                    const int kb1 = min(kvb, kb0 + split);
-                    const int b = size_bucket(kb1 - kb0, split);
-                    const long long idx = (long long)s_bucket_base[b] + atomicAdd(&s_bucket_cursor[b], 1);
-                    if (idx >= a.items_cap) continue;
-                    WorkItem w;
-                    w.a = make_int4(r, mt, h, s);
-                    w.b = make_int4(kb0, kb1, prow0, q0);
-                    w.c = make_int4(n, L, kv_end, tile);
-                    w.d = make_int4(ns, nv, 0, 0);
-                    a.items[idx] = w;
-                }
+            GroupRec rec;
+            rec.a = make_int4(r, mt, q0, n);
+            rec.b = make_int4(L, tile_kv_end(n, L, g, mt), kvb, nv);
+            rec.c = make_int4(ns, ns > 1 ? row0 : -1, 0, 0);
+            a.group_rec[gi] = rec;
+            s_place[tid] = make_int4(full0, tail0, ns, 0);
+        }
+        __syncthreads();
+        // Items of this chunk of groups, one (group, kv head) pair per thread.
+        const int chunk_groups = min(kPlanThreads, n_groups - base);
+        for (int p = tid; p < chunk_groups * Hkv; p += kPlanThreads) {
+            const int lg = p / Hkv, h = p - lg * Hkv;
+            const int4 pl = s_place[lg];
+            const int gq = base + lg, ns_g = pl.z;
+            if (ns_g > 1) a.tile_counter[gq * Hkv + h] = 0;
+            for (int s = 0; s < ns_g; ++s) {
+                const long long idx = s < ns_g - 1 ? (long long)pl.x + h * (ns_g - 1) + s : (long long)pl.y + h;
+                if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, 0);
             }
         }
+        __syncthreads();
         row_carry += tot_rows;
     }
     if (tid == 0) a.header->n_partial_rows = row_carry;
 
     // 5. chunk items, longest first.
-    for (int gi = tid; gi < n_cgroups; gi += kPlanThreads) {
-        const int r = find_group_request(req_c, R, gi);
-        const int mt = gi - req_c[r];
+    for (int base = 0; base < n_cgroups; base += kPlanThreads) {
+        const int gi = base + tid;
+        int r = 0, mt = 0, kv_end = 0, b = -1;
+        if (gi < n_cgroups) {
+            r = find_group_request(req_c, R, gi);
+            mt = gi - req_c[r];
+            kv_end = chunk_kv_end(r, mt);
+            b = chunk_bucket(kv_end);
+        }
+        const int first = (b >= 0 ? s_cbucket_base[b] : 0) + warp_claim(b, Hkv, s_cbucket_cursor);
+        if (gi >= n_cgroups) continue;
         const int n = req_n[r];
         const long long rows = (long long)n * g;
-        const int kv_end = chunk_kv_end(r, mt);
         const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
-        const int b = chunk_bucket(kv_end);
         for (int h = 0; h < Hkv; ++h) {
-            const int idx = s_cbucket_base[b] + atomicAdd(&s_cbucket_cursor[b], 1);
+            const int idx = first + h;
             ChunkItem c;
             c.a = make_int4(r, mt, h, kv_end);
             c.b = make_int4(req_q0[r], n, req_L[r], nv);
@@ -362,6 +415,7 @@ struct DecodeArgs {
     int max_blocks_per_req, num_blocks, num_q_heads, num_kv_heads, group;
     float scale_log2;
     const WorkItem *items;
+    const GroupRec *group_rec;
     WsHeader *header;
     int32_t *tile_counter;
     float2 *part_ml;
@@ -441,6 +495,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     const int n_items = a.header->n_items;
+    const int split = a.header->split_blocks;
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -460,13 +515,16 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                 mbar_arrive(&qfull[qb]);
                 break;
             }
-            const WorkItem w = a.items[cur];
+            const int4 w = a.items[cur].v;
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);  // next item, fetched early
-            const int r = w.a.x, mt = w.a.y, h = w.a.z, s = w.a.w;
-            const int kb0 = w.b.x, kb1 = w.b.y, q0 = w.b.w;
-            const int n = w.c.x, L = w.c.y, kv_end = w.c.z;
-            const int nv = w.d.y;
+            const int gi = w.x, h = w.y, s = w.z;
+            const GroupRec G = a.group_rec[gi];
+            const int r = G.a.x, mt = G.a.y, q0 = G.a.z, n = G.a.w;
+            const int L = G.b.x, kv_end = G.b.y, kvb = G.b.z, nv = G.b.w;
+            const int ns = G.c.x;
+            const int kb0 = s * split, kb1 = min(kvb, kb0 + split);
+            const int prow0 = ns > 1 ? G.c.y + h * ns * nv : -1;
 
             // Item description: rows (token, q head, last visible key).
             if (lane < kRowsPerTile) {
@@ -478,8 +536,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                 d.row_limit[lane] = valid ? L - n + i : kv_end - 1;
             }
             if (lane == 0) {
-                d.item = cur; d.kb0 = kb0; d.kb1 = kb1; d.part_row0 = w.b.z; d.n_valid = nv;
-                d.kv_end = kv_end; d.s = s; d.ns = w.d.x; d.tile = w.c.w;
+                d.item = cur; d.kb0 = kb0; d.kb1 = kb1; d.part_row0 = prow0; d.n_valid = nv;
+                d.kv_end = kv_end; d.s = s; d.ns = ns; d.tile = gi * Hkv + h;
             }
             __syncwarp();
             // Q rows: one bulk copy per run of rows that belong to one token
@@ -959,6 +1017,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.group_kvb = reinterpret_cast<int32_t *>(ws + L.group_kvb);
     pa.tile_counter = reinterpret_cast<int32_t *>(ws + L.tile_counter);
     pa.items = reinterpret_cast<WorkItem *>(ws + L.items);
+    pa.group_rec = reinterpret_cast<GroupRec *>(ws + L.group_rec);
     int plan_smem = 0;
     if (num_reqs <= kPlanSmemReqs) {
         plan_smem = kReqCacheArrays * (num_reqs + 1) * 4;
@@ -980,6 +1039,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     da.group = num_q_heads / Hkv;
     da.scale_log2 = scale * kLog2e;
     da.items = pa.items;
+    da.group_rec = pa.group_rec;
     da.header = header;
     da.tile_counter = pa.tile_counter;
     da.part_ml = reinterpret_cast<float2 *>(ws + L.part_ml);

@@ -60,14 +60,20 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// a = {r, mt, h, s}, b = {kb0, kb1, part_row0 or -1, qstart},
-// c = {n, L, kv_end, tile}, d = {ns, n_valid, 0, 0}.
+// One split-KV work item: {group, kv head h, split s, 0}. The rest lives in
+// the group's record, written once per group.
 struct WorkItem {
-    int4 a, b, c, d;
+    int4 v;
+};
+
+// a = {r, mt, qstart, n}, b = {L, kv_end, kv blocks, valid rows},
+// c = {splits ns, first partial row of kv head 0 (or -1), 0, 0}.
+struct GroupRec {
+    int4 a, b, c;
 };
 
 struct WsLayout {
-    size_t req_cache, group_req, group_kvb, tile_counter, items, chunk_items, part_ml, part_o, total;
+    size_t req_cache, group_req, group_kvb, group_rec, tile_counter, items, chunk_items, part_ml, part_o, total;
     long long groups_cap, tiles_cap, items_cap, chunk_items_cap, part_rows_cap;
 };
 
@@ -88,6 +94,7 @@ inline WsLayout ws_layout(long long num_reqs, long long num_tokens, int num_q_he
     L.req_cache = off;    off = align256(off + sizeof(int32_t) * kReqCacheArrays * (num_reqs + 1));
     L.group_req = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
     L.group_kvb = off;    off = align256(off + sizeof(int32_t) * L.groups_cap);
+    L.group_rec = off;    off = align256(off + sizeof(GroupRec) * L.groups_cap);
     L.tile_counter = off; off = align256(off + sizeof(int32_t) * L.tiles_cap);
     L.items = off;        off = align256(off + sizeof(WorkItem) * L.items_cap);
     L.chunk_items = off;  off = align256(off + 32 * L.chunk_items_cap);
