@@ -58,6 +58,8 @@ struct PlanArgs {
     WorkItem *items;
     GroupRec *group_rec;
     ChunkItem *chunk_items;
+    const int32_t *block_table;
+    int4 *prefix_map;  // per global row T_r * g + j: {slot-0 partial row at kv head 0, row stride per kv head, group, arrivals}
 };
 
 // Exclusive scan over the 1024 threads of the block; *total gets the sum.
@@ -137,6 +139,34 @@ __device__ __forceinline__ int warp_claim(int key, int per, int *counters) {
     return base + per * __popc(peers & ((1u << lane) - 1u));
 }
 
+// Smallest j < pcap with table[r][j] != table[0][j] over this thread's
+// share of the pairs (r >= 1, j), INT_MAX if none; eight independent loads
+// per pass.
+template <typename I>
+__device__ __forceinline__ int first_table_diff(const int32_t *bt0, long long mbr, I total, int pcap) {
+    int first = INT_MAX;
+    for (I e0 = threadIdx.x; e0 < total; e0 += (I)8 * blockDim.x) {
+        int x[8], y[8], jj[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const I e = e0 + (I)k * blockDim.x;
+            x[k] = y[k] = 0;
+            jj[k] = INT_MAX;
+            if (e < total) {
+                const I rr = e / pcap;
+                const int j = (int)(e - rr * pcap);
+                x[k] = __ldg(bt0 + (long long)(rr + 1) * mbr + j);
+                y[k] = __ldg(bt0 + j);
+                jj[k] = j;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (x[k] != y[k]) first = min(first, jj[k]);
+    }
+    return first;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     // Dynamic shared memory: the per-request tables when the batch has at
     // most kPlanSmemReqs requests, then the per-group tables when there are
@@ -144,8 +174,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     extern __shared__ int32_t s_dyn[];
     __shared__ long long s_ll[32];
     __shared__ unsigned long long s_ull[32];
-    __shared__ int s_i[32];
     __shared__ int s_split, s_kvmax, s_full_total, s_full_count;
+    __shared__ int s_pcap, s_pfx, s_cas_ok;  // shared-prefix pass: cap, blocks found, still possible
     __shared__ int4 s_place[kPlanThreads];  // per group of a chunk: first full-split item, first tail item, splits
     __shared__ int s_bucket_count[kSizeBuckets], s_bucket_base[kSizeBuckets], s_bucket_cursor[kSizeBuckets];
     __shared__ int s_cbucket_count[kSizeBuckets], s_cbucket_base[kSizeBuckets], s_cbucket_cursor[kSizeBuckets];
@@ -171,6 +201,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.header->next_chunk_item = 0;
         a.header->diag = 0;
         s_kvmax = 0;
+        s_pcap = kCascadeMaxBlocks;
+        s_cas_ok = R >= kCascadeMinReqs ? 1 : 0;
     }
     if (tid < kSizeBuckets) {
         s_cbucket_count[tid] = 0;
@@ -188,7 +220,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         unsigned long long tiles = 0;
         if (r < R) {
             const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
-            if ((r == 0 && q0 != 0) || (r == R - 1 && q1 != a.num_tokens)) atomicOr(status, PKV_DEV_BAD_QSL);
+            // block 0 of every table against request 0's (the shared-prefix test)
+            if (r > 0 && __ldg(a.block_table + (long long)r * a.max_blocks_per_req) != __ldg(a.block_table))
+                s_cas_ok = 0;
+            if ((r == 0 && q0 != 0) || (r == R - 1 && q1 != a.num_tokens)) {
+                atomicOr(status, PKV_DEV_BAD_QSL);
+                s_cas_ok = 0;  // some token would belong to no request
+            }
             const int n = q1 - q0;
             bool ok = false;
             if (n < 0 || q0 < 0 || q1 > a.num_tokens) {
@@ -201,10 +239,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
                 if (a.chunk_ok && rows >= kChunkRows) {
                     tiles = (unsigned long long)((rows + kChunkRows - 1) / kChunkRows) << 32;
                     atomicMax(&s_kvmax, L);
+                    s_cas_ok = 0;  // the shared-prefix pass covers split-KV rows only
                 } else {
                     tiles = (unsigned long long)((rows + kRowsPerTile - 1) / kRowsPerTile);
                 }
+                // shared blocks must hold only keys every query row sees
+                atomicMin(&s_pcap, (L - n) / PKV_BLOCK_SIZE);
             }
+            if (!ok) s_cas_ok = 0;
             req_n[r] = ok ? n : 0;
             req_L[r] = L;
             req_q0[r] = q0;
@@ -234,8 +276,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) {
         req_g[R] = n_groups;
         req_c[R] = n_cgroups;
+        s_pfx = (s_cas_ok && s_pcap >= kCascadeMinBlocks) ? s_pcap : 0;
     }
     __syncthreads();
+
+    // 1b. shared prefix: the leading block ids every table has in common.
+    if (s_pfx > 0) {
+        const int pcap = s_pfx;
+        const int32_t *bt0 = a.block_table;
+        const long long mbr = a.max_blocks_per_req;
+        __syncthreads();  // every thread has read pcap before any lowers s_pfx
+        const long long total = (long long)(R - 1) * pcap;
+        const bool small = total <= (long long)INT_MAX - 16LL * kPlanThreads;  // int indexes cannot wrap
+        const int first_diff = small ? first_table_diff<int>(bt0, mbr, (int)total, pcap)
+                                     : first_table_diff<long long>(bt0, mbr, total, pcap);
+        if (first_diff != INT_MAX) atomicMin(&s_pfx, first_diff);
+        __syncthreads();
+        if (tid == 0 && s_pfx < kCascadeMinBlocks) s_pfx = 0;
+        __syncthreads();
+    }
+    const int P0 = s_pfx;
 
     // 2. keys per decode group, total work in block loads; chunk buckets.
     long long work = 0;
@@ -245,8 +305,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         const int kvb = (tile_kv_end(req_n[r], req_L[r], g, mt) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
         grp_req[gi] = r;
         grp_kvb[gi] = kvb;
-        work += (long long)kvb * Hkv;
+        work += (long long)(kvb - P0) * Hkv;
     }
+    if (tid == 0 && P0 > 0)  // the prefix tiles
+        work += ((long long)a.num_tokens * g + kRowsPerTile - 1) / kRowsPerTile * Hkv * P0;
     const int kvmax = s_kvmax;
     auto chunk_kv_end = [&](int r, int mt) {
         const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
@@ -275,24 +337,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         if (a.part_rows_cap <= 0) sp = INT_MAX / 2;
         s_split = (int)min(sp, (long long)(INT_MAX / 2));
     }
+    // With a shared prefix every tile also gets partial slot 0 for the
+    // prefix pass, so it always takes the partial path; its splits cover
+    // only the blocks after the prefix. If the partial rows cannot fit even
+    // unsplit, the prefix pass is dropped.
     while (true) {
         if (tid < kSizeBuckets) s_bucket_count[tid] = 0;
         if (tid == 0) s_full_count = 0;
         __syncthreads();
-        const int split = s_split;
+        const int split = s_split, Pl = s_pfx;
         long long rows = 0;
         for (int base = 0; base < n_groups; base += kPlanThreads) {
             const int gi = base + tid;
             int full = 0, tail_key = -1;
             if (gi < n_groups) {
-                const int kvb = grp_kvb[gi];
-                const int ns = max(1, (kvb + split - 1) / split);
-                if (ns > 1) {
+                const int sb = grp_kvb[gi] - Pl;
+                const int ns = max(1, (sb + split - 1) / split);
+                const int slots = ns + (Pl > 0 ? 1 : 0);
+                if (slots > 1) {
                     const int r = grp_req[gi];
-                    rows += (long long)ns * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
-                    full = (ns - 1) * Hkv;
+                    rows += (long long)slots * Hkv * tile_rows(req_n[r], g, gi - req_g[r]);
                 }
-                tail_key = size_bucket(kvb - (ns - 1) * split, split);
+                full = (ns - 1) * Hkv;
+                tail_key = size_bucket(sb - (ns - 1) * split, split);
             }
             const int full_warp = __reduce_add_sync(0xffffffffu, full);
             if ((tid & 31) == 0 && full_warp) {
@@ -303,9 +370,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         }
         rows = block_sum<long long>(rows, s_ll);
         if (rows <= a.part_rows_cap) break;
-        if (tid == 0) s_split = split > INT_MAX / 4 ? INT_MAX / 2 : split * 2;
+        if (tid == 0) {
+            if (split < INT_MAX / 2) s_split = split > INT_MAX / 4 ? INT_MAX / 2 : split * 2;
+            else s_pfx = 0;  // cannot happen without a prefix: unsplit tiles need no partial rows
+        }
     }
     const int split = s_split;
+    const int P = s_pfx;
     if (tid == 0) {
         s_full_total = s_full_count;
         s_bucket_cursor[0] = 0;
@@ -321,6 +392,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.header->n_chunk_items = cacc;
         a.header->split_blocks = split;
         a.header->n_groups = n_groups;
+        a.header->cascade_blocks = P;
+        a.header->n_prefix_items =
+            P > 0 ? (int)(((long long)a.num_tokens * g + kRowsPerTile - 1) / kRowsPerTile) * Hkv : 0;
     }
     __syncthreads();
 
@@ -329,14 +403,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     for (int base = 0; base < n_groups; base += kPlanThreads) {
         const int gi = base + tid;
         int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
+        int slots = 0;
         if (gi < n_groups) {
             r = grp_req[gi];
             mt = gi - req_g[r];
             kvb = grp_kvb[gi];
-            ns = max(1, (kvb + split - 1) / split);
+            ns = max(1, (kvb - P + split - 1) / split);
+            slots = ns + (P > 0 ? 1 : 0);
             nv = tile_rows(req_n[r], g, mt);
         }
-        const int n_rows = (gi < n_groups && ns > 1) ? ns * Hkv * nv : 0;
+        const int n_rows = (gi < n_groups && slots > 1) ? slots * Hkv * nv : 0;
         const int full_cnt = gi < n_groups ? (ns - 1) * Hkv : 0;
         // One scan carries the partial rows (low half) and the full-size
         // split items (high half); both totals are within int range once the
@@ -348,7 +424,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         const int tot_rows = (int)(tot & 0xffffffffu);
         const int full0 = s_bucket_base[0] + full_carry + (int)(ex >> 32);
         full_carry += (int)(tot >> 32);
-        const int tail_b = gi < n_groups ? size_bucket(kvb - (ns - 1) * split, split) : -1;
+        const int tail_b = gi < n_groups ? size_bucket(kvb - P - (ns - 1) * split, split) : -1;
         // tail items of bucket 0 come after every full-size split
         const int tail0 = (tail_b > 0 ? s_bucket_base[tail_b] : s_bucket_base[0] + s_full_total) +
                           warp_claim(tail_b, Hkv, s_bucket_cursor);
@@ -357,9 +433,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             GroupRec rec;
             rec.a = make_int4(r, mt, q0, n);
             rec.b = make_int4(L, tile_kv_end(n, L, g, mt), kvb, nv);
-            rec.c = make_int4(ns, ns > 1 ? row0 : -1, 0, 0);
+            // arrivals: the splits, plus the prefix tiles over its rows
+            const long long grow0 = (long long)q0 * g + (long long)mt * kRowsPerTile;
+            const int arrivals =
+                ns + (P > 0 ? (int)((grow0 + nv - 1) / kRowsPerTile - grow0 / kRowsPerTile) + 1 : 0);
+            rec.c = make_int4(ns, slots > 1 ? row0 : -1, slots, arrivals);
             a.group_rec[gi] = rec;
-            s_place[tid] = make_int4(full0, tail0, ns, 0);
+            if (P > 0) {  // the prefix-tile view of this group's rows
+                int4 *m = a.prefix_map + grow0;
+                for (int row = 0; row < nv; ++row) m[row] = make_int4(row0 + row, slots * nv, gi, arrivals);
+            }
+            s_place[tid] = make_int4(full0, tail0, ns, slots);
         }
         __syncthreads();
         // Items of this chunk of groups, one (group, kv head) pair per thread.
@@ -368,7 +452,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             const int lg = p / Hkv, h = p - lg * Hkv;
             const int4 pl = s_place[lg];
             const int gq = base + lg, ns_g = pl.z;
-            if (ns_g > 1) a.tile_counter[gq * Hkv + h] = 0;
+            if (pl.w > 1) a.tile_counter[gq * Hkv + h] = 0;
             for (int s = 0; s < ns_g; ++s) {
                 const long long idx = s < ns_g - 1 ? (long long)pl.x + h * (ns_g - 1) + s : (long long)pl.y + h;
                 if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, 0);
@@ -416,6 +500,8 @@ struct DecodeArgs {
     float scale_log2;
     const WorkItem *items;
     const GroupRec *group_rec;
+    const int4 *prefix_map;
+    int num_tokens;
     WsHeader *header;
     int32_t *tile_counter;
     float2 *part_ml;
@@ -424,11 +510,17 @@ struct DecodeArgs {
 
 // Per-item description handed from the producer to the consumers through
 // shared memory, next to the item's Q rows. item < 0 ends the CTA's loop.
+// A split item's rows all belong to one decode tile; a prefix-tile item's
+// rows may belong to up to 16 (row_tile: the tile's counter, -1 past
+// n_valid).
 struct ItemDesc {
-    int item, kb0, kb1, part_row0, n_valid, kv_end, s, ns, tile, pad[7];
+    int item, kb0, kb1, n_valid, kv_end, partial, prefix, slots, part_row0, pad[7];
     int row_t[kRowsPerTile];
     int row_hq[kRowsPerTile];
     int row_limit[kRowsPerTile];
+    int row_prow[kRowsPerTile];  // partial row this item writes for the row (when partial)
+    int row_tile[kRowsPerTile];  // the row's tile counter (-1 past n_valid)
+    int row_arr[kRowsPerTile];   // arrivals that tile waits for
 };
 
 template <int D>
@@ -460,6 +552,129 @@ __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, 
         : "memory");
 }
 
+// One work item on the producer warp: its description (rows, key range,
+// where the result goes), its Q rows and its K/V block tiles through the
+// ring. Prefix tiles and split items get separate copies of the streaming
+// loop. Returns false when a wait gave up.
+template <int D, bool kPrefix>
+__device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const DecodeArgs &a, uint8_t *smem, ItemDesc &d,
+                                             int qb, int cur, int n_prefix, int split, int P, uint64_t *bar,
+                                             uint32_t &e, int32_t *status, volatile int *abort) {
+    using S = DecodeSmem<D>;
+    uint64_t *full = bar, *empty = bar + S::kStages, *qfull = bar + 2 * S::kStages;
+    const int lane = threadIdx.x & 31;
+    const int Hkv = a.num_kv_heads, g = a.group;
+    bool ok = true;
+    int r, mt, q0, nv, kb0, kb1, kv_end, h;
+    if constexpr (kPrefix) {
+        // Prefix tile: global rows [pt * 16, +16) over the shared
+        // blocks [0, P), which every row sees whole.
+        const int pt = cur / Hkv;
+        h = cur - pt * Hkv;
+        r = 0; mt = pt; q0 = 0;
+        nv = (int)min((long long)kRowsPerTile, (long long)a.num_tokens * g - (long long)pt * kRowsPerTile);
+        kb0 = 0; kb1 = P; kv_end = P * PKV_BLOCK_SIZE;
+        if (lane < kRowsPerTile) {
+            const int rho = pt * kRowsPerTile + lane;
+            const bool valid = lane < nv;
+            d.row_t[lane] = valid ? rho / g : 0;
+            d.row_hq[lane] = h * g + (valid ? rho % g : 0);
+            d.row_limit[lane] = kv_end - 1;
+            const int4 m = valid ? a.prefix_map[rho] : make_int4(0, 0, -1, 0);
+            d.row_prow[lane] = m.x + h * m.y;
+            d.row_tile[lane] = valid ? m.z * Hkv + h : -1;
+            d.row_arr[lane] = m.w;
+        }
+        if (lane == 0) { d.partial = 1; d.prefix = 1; }
+    } else {
+        const int4 w = a.items[cur - n_prefix].v;
+        const int gi = w.x, s = w.z;
+        h = w.y;
+        const GroupRec G = a.group_rec[gi];
+        r = G.a.x; mt = G.a.y; q0 = G.a.z;
+        const int n = G.a.w, L = G.b.x, kvb = G.b.z, slots = G.c.z;
+        nv = G.b.w;
+        kv_end = G.b.y;
+        kb0 = P + s * split;
+        kb1 = min(kvb, kb0 + split);
+        // Rows: token, q head, last visible key, partial row.
+        if (lane < kRowsPerTile) {
+            const int rho = mt * kRowsPerTile + lane;
+            const bool valid = lane < nv;
+            const int i = valid ? rho / g : 0;
+            d.row_t[lane] = q0 + i;
+            d.row_hq[lane] = h * g + (valid ? rho % g : 0);
+            d.row_limit[lane] = valid ? L - n + i : kv_end - 1;
+            d.row_prow[lane] = G.c.y + (h * slots + s + slots - G.c.x) * nv + lane;
+            d.row_tile[lane] = valid ? gi * Hkv + h : -1;
+            d.row_arr[lane] = G.c.w;
+        }
+        if (lane == 0) {
+            d.partial = slots > 1; d.prefix = 0; d.slots = slots; d.part_row0 = G.c.y + h * slots * nv;
+        }
+    }
+    if (lane == 0) {
+        d.item = cur; d.kb0 = kb0; d.kb1 = kb1; d.n_valid = nv; d.kv_end = kv_end;
+    }
+    __syncwarp();
+    // Q rows: one bulk copy per run of rows that belong to one token
+    // (consecutive q heads, contiguous in q).
+    uint8_t *qs = smem + S::kOffQ + qb * S::kQBytes;
+    if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], (uint32_t)nv * D * 2);
+    __syncwarp();
+    if (lane < nv) {
+        const int rho = mt * kRowsPerTile + lane;
+        const int i = rho / g;
+        const bool run_start = lane == 0 || (rho - 1) / g != i;
+        if (run_start) {
+            int len = 1;
+            while (lane + len < nv && (rho + len) / g == i) ++len;
+            const __nv_bfloat16 *src = a.q + ((long long)(q0 + i) * a.num_q_heads + h * g + rho % g) * D;
+            bulk_copy_g2s(qs + lane * S::kQStride, src, (uint32_t)len * D * 2, &qfull[qb]);
+        }
+    }
+    if (lane != 0) mbar_arrive(&qfull[qb]);
+
+    // K/V block tiles through the ring; block-table entries are
+    // fetched 32 at a time, one batch ahead.
+    const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
+    auto fetch = [&](int base) {
+        int b = 0;
+        if (base + lane < kb1) {
+            b = __ldg(bt + base + lane);
+            if (b < 0 || b >= a.num_blocks) {
+                raise_status(status, PKV_DEV_BAD_BLOCK);
+                b = a.num_blocks;  // outside the tensor map: TMA fills zeros
+            }
+        }
+        return b;
+    };
+    int my_blk = fetch(kb0);
+    for (int base = kb0; base < kb1 && ok; base += 32) {
+        const int nxt_blk = fetch(base + 32);
+        const int cnt = min(32, kb1 - base);
+        for (int j = 0; j < cnt; ++j) {
+            const int blk = __shfl_sync(0xffffffffu, my_blk, j);
+            const int stage = e % S::kStages;
+            if (!mbar_wait(&empty[stage], ((e / S::kStages) & 1) ^ 1, status, abort)) { ok = false; break; }
+            if (lane == 0) {
+                uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
+                mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+#pragma unroll
+                for (int bx = 0; bx < S::kBoxes; ++bx) {
+                    tma_load_3d(st + bx * 2048, kv_map, bx * 64, h * PKV_BLOCK_SIZE, blk, &full[stage]);
+                    tma_load_3d(st + S::kTileBytes + bx * 2048, kv_map, bx * 64,
+                                (Hkv + h) * PKV_BLOCK_SIZE, blk, &full[stage]);
+                }
+            }
+            __syncwarp();
+            ++e;
+        }
+        my_blk = nxt_blk;
+    }
+    return ok;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, D == 128 ? 2 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
@@ -467,7 +682,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;  // set by any wait that gives up; every later wait returns at once
     __shared__ int s_stop;   // consumers' uniform loop decision, written by consumer thread 0
-    __shared__ int s_last;   // this CTA finished a tile's last split
+    __shared__ int s_last;   // rows of this item whose tile it finished (bit per row)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *full = bar, *empty = bar + S::kStages, *qfull = bar + 2 * S::kStages, *qempty = qfull + 2;
@@ -494,13 +709,14 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     // wrote is read only after this.
     pdl_wait();
     pdl_launch_dependents();
-    const int n_items = a.header->n_items;
+    const int n_prefix = a.header->n_prefix_items;
+    const int n_items = n_prefix + a.header->n_items;
     const int split = a.header->split_blocks;
+    const int P = a.header->cascade_blocks;
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) tma_prefetch_desc(&kv_map);
-        const int Hkv = a.num_kv_heads, g = a.group;
         uint32_t e = 0;  // ring element counter
         bool ok = true;
         int cur = 0;
@@ -515,86 +731,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                 mbar_arrive(&qfull[qb]);
                 break;
             }
-            const int4 w = a.items[cur].v;
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);  // next item, fetched early
-            const int gi = w.x, h = w.y, s = w.z;
-            const GroupRec G = a.group_rec[gi];
-            const int r = G.a.x, mt = G.a.y, q0 = G.a.z, n = G.a.w;
-            const int L = G.b.x, kv_end = G.b.y, kvb = G.b.z, nv = G.b.w;
-            const int ns = G.c.x;
-            const int kb0 = s * split, kb1 = min(kvb, kb0 + split);
-            const int prow0 = ns > 1 ? G.c.y + h * ns * nv : -1;
-
-            // Item description: rows (token, q head, last visible key).
-            if (lane < kRowsPerTile) {
-                const int rho = mt * kRowsPerTile + lane;
-                const bool valid = lane < nv;
-                const int i = valid ? rho / g : 0;
-                d.row_t[lane] = q0 + i;
-                d.row_hq[lane] = h * g + (valid ? rho % g : 0);
-                d.row_limit[lane] = valid ? L - n + i : kv_end - 1;
-            }
-            if (lane == 0) {
-                d.item = cur; d.kb0 = kb0; d.kb1 = kb1; d.part_row0 = prow0; d.n_valid = nv;
-                d.kv_end = kv_end; d.s = s; d.ns = ns; d.tile = gi * Hkv + h;
-            }
-            __syncwarp();
-            // Q rows: one bulk copy per run of rows that belong to one token
-            // (consecutive q heads, contiguous in q).
-            uint8_t *qs = smem + S::kOffQ + qb * S::kQBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], (uint32_t)nv * D * 2);
-            __syncwarp();
-            if (lane < nv) {
-                const int rho = mt * kRowsPerTile + lane;
-                const int i = rho / g;
-                const bool run_start = lane == 0 || (rho - 1) / g != i;
-                if (run_start) {
-                    int len = 1;
-                    while (lane + len < nv && (rho + len) / g == i) ++len;
-                    const __nv_bfloat16 *src = a.q + ((long long)(q0 + i) * a.num_q_heads + h * g + rho % g) * D;
-                    bulk_copy_g2s(qs + lane * S::kQStride, src, (uint32_t)len * D * 2, &qfull[qb]);
-                }
-            }
-            if (lane != 0) mbar_arrive(&qfull[qb]);
-
-            // K/V block tiles through the ring; block-table entries are
-            // fetched 32 at a time, one batch ahead.
-            const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
-            auto fetch = [&](int base) {
-                int b = 0;
-                if (base + lane < kb1) {
-                    b = __ldg(bt + base + lane);
-                    if (b < 0 || b >= a.num_blocks) {
-                        raise_status(status, PKV_DEV_BAD_BLOCK);
-                        b = a.num_blocks;  // outside the tensor map: TMA fills zeros
-                    }
-                }
-                return b;
-            };
-            int my_blk = fetch(kb0);
-            for (int base = kb0; base < kb1 && ok; base += 32) {
-                const int nxt_blk = fetch(base + 32);
-                const int cnt = min(32, kb1 - base);
-                for (int j = 0; j < cnt; ++j) {
-                    const int blk = __shfl_sync(0xffffffffu, my_blk, j);
-                    const int stage = e % S::kStages;
-                    if (!mbar_wait(&empty[stage], ((e / S::kStages) & 1) ^ 1, status, abort)) { ok = false; break; }
-                    if (lane == 0) {
-                        uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
-                        mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-#pragma unroll
-                        for (int bx = 0; bx < S::kBoxes; ++bx) {
-                            tma_load_3d(st + bx * 2048, &kv_map, bx * 64, h * PKV_BLOCK_SIZE, blk, &full[stage]);
-                            tma_load_3d(st + S::kTileBytes + bx * 2048, &kv_map, bx * 64,
-                                        (Hkv + h) * PKV_BLOCK_SIZE, blk, &full[stage]);
-                        }
-                    }
-                    __syncwarp();
-                    ++e;
-                }
-                my_blk = nxt_blk;
-            }
+            ok = cur < n_prefix
+                     ? produce_item<D, true>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status, abort)
+                     : produce_item<D, false>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status,
+                                              abort);
             if (!ok) break;
             cur = __shfl_sync(0xffffffffu, nxt, 0);
         }
@@ -778,9 +920,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             }
         }
         named_barrier_sync(1, kConsumerWarps * 32);
-        const int n_valid = d.n_valid, ns = d.ns;
+        const int n_valid = d.n_valid;
+        const bool partial = d.partial != 0;
         constexpr int kC4 = D / 4;
-        const long long prow_s = (long long)d.part_row0 + (long long)d.s * n_valid;
         for (int idx = tid; idx < n_valid * kC4; idx += kConsumerWarps * 32) {
             const int row = idx / kC4, c4 = idx % kC4;
             float M = -INFINITY;
@@ -799,7 +941,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                     acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
                 }
             }
-            if (ns <= 1) {
+            if (!partial) {
                 const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
                 const long long off = ((long long)d.row_t[row] * a.num_q_heads + d.row_hq[row]) * D + c4 * 4;
                 uint2 pk;
@@ -807,42 +949,76 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                 pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
                 *reinterpret_cast<uint2 *>(a.out + off) = pk;
             } else {
-                const long long prow = prow_s + row;
+                const long long prow = d.row_prow[row];
                 *reinterpret_cast<float4 *>(a.part_o + prow * D + c4 * 4) = acc;
                 if (c4 == 0) a.part_ml[prow] = make_float2(M, lsum);
             }
         }
-        if (ns > 1) {
-            // Publish this split, then count it; the CTA that brings the
-            // count to ns merges every split of the tile (no waiting).
+        if (partial) {
+            // Publish the partial rows, then count one arrival at each tile
+            // they belong to (the first row of each run of equal tiles
+            // counts); the CTA that brings a tile's count to its arrivals
+            // merges the tile (no waiting).
             __threadfence();
             named_barrier_sync(1, kConsumerWarps * 32);
-            if (tid == 0) s_last = atomicAdd(&a.tile_counter[d.tile], 1) == ns - 1;
+            if (warp == 0) {
+                bool last = false;
+                if (lane < n_valid) {
+                    const int tile = d.row_tile[lane];
+                    if (lane == 0 || d.row_tile[lane - 1] != tile)
+                        last = atomicAdd(&a.tile_counter[tile], 1) == d.row_arr[lane] - 1;
+                }
+                const unsigned mask = __ballot_sync(0xffffffffu, last);
+                if (lane == 0) s_last = (int)mask;
+            }
             named_barrier_sync(1, kConsumerWarps * 32);
-            if (s_last) {
-                __threadfence();
-                const long long prow0 = d.part_row0;
-                for (int idx = tid; idx < n_valid * kC4; idx += kConsumerWarps * 32) {
+            unsigned todo = (unsigned)s_last;
+            if (todo) __threadfence();
+            while (todo) {
+                const int tile = d.row_tile[__ffs(todo) - 1];
+                todo &= todo - 1;
+                // A split item merges its own tile (all in the description);
+                // a prefix tile looks up the tile it completed.
+                const int g = a.group;
+                int h, mt = 0, q0 = 0, nv = n_valid, slots = d.slots;
+                long long prow0 = d.part_row0;
+                const bool pfx = d.prefix != 0;
+                if (pfx) {
+                    const int gi = tile / a.num_kv_heads;
+                    h = tile - gi * a.num_kv_heads;
+                    const GroupRec G = a.group_rec[gi];
+                    mt = G.a.y; q0 = G.a.z; nv = G.b.w; slots = G.c.z;
+                    prow0 = G.c.y + (long long)h * slots * nv;
+                } else {
+                    h = tile % a.num_kv_heads;
+                }
+                for (int idx = tid; idx < nv * kC4; idx += kConsumerWarps * 32) {
                     const int row = idx / kC4, c4 = idx % kC4;
                     float M = -INFINITY;
-                    for (int sp = 0; sp < ns; ++sp)
-                        M = fmaxf(M, __ldcg(&a.part_ml[prow0 + (long long)sp * n_valid + row]).x);
+                    for (int sp = 0; sp < slots; ++sp)
+                        M = fmaxf(M, __ldcg(&a.part_ml[prow0 + (long long)sp * nv + row]).x);
                     float lsum = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int sp = 0; sp < ns; ++sp) {
-                        const long long prow = prow0 + (long long)sp * n_valid + row;
+                    for (int sp = 0; sp < slots; ++sp) {
+                        const long long prow = prow0 + (long long)sp * nv + row;
                         const float2 ml = __ldcg(&a.part_ml[prow]);
                         const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
                         lsum += ml.y * f;
                         const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_o + prow * D + c4 * 4));
                         acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
                     }
+                    long long orow;
+                    if (pfx) {
+                        const int rho = mt * kRowsPerTile + row;
+                        orow = (long long)(q0 + rho / g) * a.num_q_heads + h * g + rho % g;
+                    } else {
+                        orow = (long long)d.row_t[row] * a.num_q_heads + d.row_hq[row];
+                    }
                     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                    const long long off = ((long long)d.row_t[row] * a.num_q_heads + d.row_hq[row]) * D + c4 * 4;
                     uint2 pk;
                     pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                     pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2 *>(a.out + off) = pk;
+                    *reinterpret_cast<uint2 *>(a.out + orow * D + c4 * 4) = pk;
                 }
             }
         }
@@ -1018,6 +1194,8 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.tile_counter = reinterpret_cast<int32_t *>(ws + L.tile_counter);
     pa.items = reinterpret_cast<WorkItem *>(ws + L.items);
     pa.group_rec = reinterpret_cast<GroupRec *>(ws + L.group_rec);
+    pa.block_table = block_table;
+    pa.prefix_map = reinterpret_cast<int4 *>(ws + L.prefix_map);
     int plan_smem = 0;
     if (num_reqs <= kPlanSmemReqs) {
         plan_smem = kReqCacheArrays * (num_reqs + 1) * 4;
@@ -1040,6 +1218,8 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     da.scale_log2 = scale * kLog2e;
     da.items = pa.items;
     da.group_rec = pa.group_rec;
+    da.prefix_map = pa.prefix_map;
+    da.num_tokens = num_tokens;
     da.header = header;
     da.tile_counter = pa.tile_counter;
     da.part_ml = reinterpret_cast<float2 *>(ws + L.part_ml);

@@ -41,6 +41,20 @@ constexpr int kPlanSmemReqs = 4096;    // per-request tables kept in shared memo
 constexpr int kPlanSmemGroups = 8192;  // per-group tables likewise, up to this many decode groups
 constexpr int kSizeBuckets = 9;      // 0 = full-size split, 1..8 = shorter, longest first
 
+// Shared prefix. When every request's block table starts with the same
+// P >= kCascadeMinBlocks blocks (a prefix-cache hit shared by the whole
+// batch) and those keys are visible to every query row, the batch's rows
+// are also cut, across request boundaries, into "prefix tiles" of 16 rows
+// (global row T_r * g + rho for token T_r of the flattened batch) that run
+// against those P blocks only: the shared blocks are read once per 16 rows
+// instead of once per request. Every decode tile then has ns + 1 partial
+// slots: slot 0 is written by the prefix tiles covering its rows, slots
+// 1..ns by its splits over the blocks [P, kv blocks); its arrival count is
+// ns plus the number of prefix tiles overlapping it.
+constexpr int kCascadeMinBlocks = 4;
+constexpr int kCascadeMinReqs = 4;
+constexpr int kCascadeMaxBlocks = 4096;
+
 // Chunk tiles (tcgen05 path): requests with at least kChunkRows query rows
 // (n * g) are cut into 128-row tiles that run over 128-key tiles.
 constexpr int kChunkRows = 128;
@@ -56,7 +70,9 @@ struct WsHeader {
     int32_t n_chunk_items;
     int32_t next_chunk_item;
     int32_t diag;          // bits naming the pipeline waits that timed out (PKV_DEV_TIMEOUT)
-    int32_t pad[55];
+    int32_t n_prefix_items; // prefix-tile items (listed before the split items; 0 without a shared prefix)
+    int32_t cascade_blocks; // P: leading blocks shared by every request (0: none)
+    int32_t pad[53];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -67,13 +83,17 @@ struct WorkItem {
 };
 
 // a = {r, mt, qstart, n}, b = {L, kv_end, kv blocks, valid rows},
-// c = {splits ns, first partial row of kv head 0 (or -1), 0, 0}.
+// c = {splits ns over the blocks after the shared prefix, first partial row
+// of kv head 0 (or -1), partial slots (ns, or ns + 1 with a shared prefix),
+// arrivals before the merge}. Kv head h's slot s holds rows
+// [c.y + (h * slots + s) * valid rows, ...).
 struct GroupRec {
     int4 a, b, c;
 };
 
 struct WsLayout {
-    size_t req_cache, group_req, group_kvb, group_rec, tile_counter, items, chunk_items, part_ml, part_o, total;
+    size_t req_cache, group_req, group_kvb, group_rec, tile_counter, items, chunk_items, prefix_map, part_ml, part_o,
+        total;
     long long groups_cap, tiles_cap, items_cap, chunk_items_cap, part_rows_cap;
 };
 
@@ -98,6 +118,7 @@ inline WsLayout ws_layout(long long num_reqs, long long num_tokens, int num_q_he
     L.tile_counter = off; off = align256(off + sizeof(int32_t) * L.tiles_cap);
     L.items = off;        off = align256(off + sizeof(WorkItem) * L.items_cap);
     L.chunk_items = off;  off = align256(off + 32 * L.chunk_items_cap);
+    L.prefix_map = off;   off = align256(off + sizeof(int4) * num_tokens * g);
     L.part_ml = off;      off = align256(off + sizeof(float2) * part_rows_cap);
     L.part_o = off;       off = align256(off + sizeof(float) * head_size * part_rows_cap);
     L.total = off;
