@@ -60,6 +60,11 @@ def parse_args():
     p.add_argument("--skip-e2e", action="store_true", help="leave out the end-to-end (host buffers) loop")
     p.add_argument("--graph", action="store_true",
                    help="replay the step from a captured CUDA graph in the timed loop")
+    p.add_argument("--l2", choices=("auto", "layers", "flush", "none"), default="auto",
+                   help="keeping L2 cold between steps. layers: consecutive steps use distinct KV pools (one "
+                        "per model layer, as a real step over a model's layers does) until their total exceeds "
+                        "512 MiB; flush: write and read 512 MiB before every step and time steps one by one; "
+                        "auto: layers when one pool is under 512 MiB, else none (the step's reads are GBs)")
     p.add_argument("--op", choices=("step", "kv_transfer"), default="step",
                    help="kv_transfer: time block gather + scatter of the workload's context blocks")
     return p.parse_args()
@@ -69,7 +74,43 @@ def parse_args():
 # workload bookkeeping (measurement only)
 # --------------------------------------------------------------------------
 
-def workload_config(batch) -> dict:
+L2_SCRUB_BYTES = 512 << 20
+
+
+def scrub_l2(scrub) -> None:
+    """Evict the step's data from L2: write a buffer four times the L2 size,
+    then read all of it back so the lines left behind are clean (no
+    write-backs land in the timed step)."""
+    import torch
+    scrub.zero_()
+    scrub.view(torch.int64).sum()
+
+
+def pool_bytes(batch) -> int:
+    s = batch.shape
+    return batch.num_blocks * 2 * 16 * s.num_kv_heads * s.head_size * 2
+
+
+def l2_mode(args, batch) -> tuple[str, int]:
+    """('layers', number of distinct pools) | ('flush', 1) | ('none', 1)."""
+    mode = args.l2
+    if mode == "auto":
+        mode = "layers" if pool_bytes(batch) < L2_SCRUB_BYTES else "none"
+    if mode == "layers":
+        return mode, max(2, -(-L2_SCRUB_BYTES // pool_bytes(batch)))
+    return mode, 1
+
+
+def l2_note(batch, mode: str, layers: int) -> str:
+    if mode == "flush":
+        return "L2 flushed before every timed step (512 MiB written then read), steps timed one by one"
+    if mode == "layers":
+        return (f"inputs larger than L2: consecutive steps rotate over {layers} distinct KV pools (one per layer, "
+                f"{layers * pool_bytes(batch) / 1e6:.0f} MB in total vs 129 MB L2), no flush")
+    return f"inputs larger than L2 (pool of {pool_bytes(batch) / 1e9:.2f} GB vs 129 MB L2), no flush"
+
+
+def workload_config(batch, l2: str = "") -> dict:
     s = batch.shape
     return {
         "workload": batch.workload,
@@ -80,7 +121,7 @@ def workload_config(batch) -> dict:
         "block_size": 16,
         "num_blocks": batch.num_blocks,
         "context_tokens": int(batch.seq_lens.sum()),
-        "l2": "inputs larger than L2 (per-step KV reads of GBs vs 129 MB L2), no flush",
+        "l2": l2 or l2_note(batch, "none", 1),
     }
 
 
@@ -377,23 +418,32 @@ def main():
         run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world)
         return
     host = host_copy(ten) if (rank == 0 and world == 1 and not args.skip_cpu_baseline) else None
-    buf = pkv.StepBuffers(batch, ten)
-    graph = pkv.StepGraph(buf) if args.graph else None
+    mode, layers = l2_mode(args, batch)
+    bufs = [pkv.StepBuffers(batch, ten)]
+    for _ in range(layers - 1):  # one pool per layer; the step's other inputs are shared
+        bufs.append(pkv.StepBuffers(batch, {**ten, "kv_cache": ten["kv_cache"].clone()}))
+    buf = bufs[0]
+    graphs = [pkv.StepGraph(b) for b in bufs] if args.graph else None
     stream = torch.cuda.current_stream()
 
     nev = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nev)]
 
-    def step(i=None):
-        pkv.paged_slot_mapping(buf.block_table, buf.seq_lens, buf.query_start_loc, buf.num_tokens,
-                               batch.num_blocks, buf.slot_mapping, buf.status)
-        pkv.paged_kv_write(buf.k, buf.v, buf.slot_mapping, buf.kv_cache, buf.status)
-        pkv.paged_attention(buf.q, buf.kv_cache, buf.block_table, buf.seq_lens, buf.query_start_loc, batch.scale,
-                            buf.out, buf.workspace, events=None if i is None else ev[i])
+    def step(i, timed_kernels=False):
+        b = bufs[i % layers]
+        if graphs is not None and not timed_kernels:
+            graphs[i % layers].replay()
+            return
+        pkv.paged_slot_mapping(b.block_table, b.seq_lens, b.query_start_loc, b.num_tokens,
+                               batch.num_blocks, b.slot_mapping, b.status)
+        pkv.paged_kv_write(b.k, b.v, b.slot_mapping, b.kv_cache, b.status)
+        pkv.paged_attention(b.q, b.kv_cache, b.block_table, b.seq_lens, b.query_start_loc, batch.scale,
+                            b.out, b.workspace, events=ev[i] if timed_kernels else None)
 
+    scrub = torch.empty(L2_SCRUB_BYTES, dtype=torch.uint8, device=dev) if mode == "flush" else None
     sampler = ClockSampler(local_rank)
-    for _ in range(args.warmup):
-        step()
+    for i in range(max(args.warmup, layers)):
+        step(i)
     # create the event handles outside the timed region
     for e4 in ev:
         for e in e4:
@@ -404,29 +454,41 @@ def main():
     torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
-    t_start.record(stream)
-    for _ in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    if scrub is not None:
+        # cold L2 every step: scrub, then time the step alone
+        ts = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            scrub_l2(scrub)
+            ts[i][0].record(stream)
+            step(i)
+            ts[i][1].record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = float(sum(a.elapsed_time(b) for a, b in ts))
+    else:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = t_start.elapsed_time(t_end)
     wall1 = time.time()
-    elapsed_ms = t_start.elapsed_time(t_end)
     # Per-kernel pass: the same K steps with events between the attention
     # launches (an event between two launches stops the next one from
     # starting early, so the headline pass above runs without them).
     for i in range(args.steps):
-        step(i)
+        if scrub is not None:
+            scrub_l2(scrub)
+        step(i, timed_kernels=True)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     sampler.stop()
-    st = pkv.pkv_read_status(buf.status)
-    wst = pkv.pkv_read_status(buf.workspace)
-    if st or wst:
-        raise RuntimeError(f"device status bits set: {st:#x} {wst:#x}")
+    for b in bufs:
+        st = pkv.pkv_read_status(b.status)
+        wst = pkv.pkv_read_status(b.workspace)
+        if st or wst:
+            raise RuntimeError(f"device status bits set: {st:#x} {wst:#x}")
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
     plan_ms = float(np.mean([e4[0].elapsed_time(e4[1]) for e4 in ev]))
@@ -438,7 +500,7 @@ def main():
     # end to end: inputs from pinned host memory, output back, every step
     e2e = None
     if not args.skip_e2e:
-        e2e = run_e2e(args, batch, ten, buf, pkv, torch, dev, dist)
+        e2e = run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub)
 
     cpu = None
     if host is not None:
@@ -461,8 +523,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block tables)",
-        "config": {**workload_config(batch), "parallelism": f"{world} independent replicas" if world > 1
-                   else "single GPU", "launch": "CUDA graph replay" if graph is not None else "eager, PDL launches"},
+        "config": {**workload_config(batch, l2_note(batch, mode, layers)), "parallelism": f"{world} independent replicas" if world > 1
+                   else "single GPU", "launch": "CUDA graph replay" if graphs is not None else "eager, PDL launches"},
         "roofline": {"bound": "hbm", "kernel": "attention decode_kernel (split-KV)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
@@ -528,49 +590,73 @@ def run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world):
         "gpu_launches": 2 * args.steps}), flush=True)
 
 
-def run_e2e(args, batch, ten, buf, pkv, torch, dev, dist):
-    """K steps through the public API with this step's inputs (q, k, v and
-    the metadata tables) copied from pinned host memory and the output copied
-    back, all inside the timed region. The pool stays resident: it is the
-    layer's KV state, not a per-step input."""
-    host_in = {
-        "q": ten["q"].cpu().pin_memory(), "k": ten["k"].cpu().pin_memory(), "v": ten["v"].cpu().pin_memory(),
-        "block_table": buf.block_table.cpu().pin_memory(), "seq_lens": buf.seq_lens.cpu().pin_memory(),
-        "query_start_loc": buf.query_start_loc.cpu().pin_memory(),
-    }
-    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True)
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = out_host.numel() * out_host.element_size()
-    slots = torch.empty(batch.num_tokens, dtype=torch.int32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
+def run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub=None):
+    """K steps through the library's host-buffer pipeline
+    (``binding.HostStepPipeline``): every step copies its inputs (q, k, v
+    and the metadata tables) from pinned host memory and its output back to
+    pinned host memory, inside the timed region; step i+1's input copies
+    overlap step i's kernels and step i's output copy overlaps step i+1's.
+    The pool stays resident: it is the layer's KV state, not a per-step
+    input; with several pools (``bufs``, one per layer) consecutive steps
+    rotate over them as in the device-resident pass. With ``scrub`` every
+    step runs alone after an L2 flush, copies included."""
+    buf = bufs[0]
+    layers = len(bufs)
+    s = batch.shape
+    pipe = pkv.HostStepPipeline(buf.kv_cache, batch.num_reqs, batch.num_tokens, batch.max_blocks_per_req,
+                                s.num_q_heads, batch.scale)
+    src = {"q": ten["q"].cpu(), "k": ten["k"].cpu(), "v": ten["v"].cpu(), "block_table": buf.block_table.cpu(),
+           "seq_lens": buf.seq_lens.cpu(), "query_start_loc": buf.query_start_loc.cpu()}
+    for slot in range(pipe.depth):  # the host producer's side: inputs written into each pinned slot once
+        views = pipe.slot_inputs(slot)
+        for k, v in src.items():
+            views[k].copy_(v)
+    outs = [torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True) for _ in range(2)]
+    h2d = pipe.packed_bytes
+    d2h = outs[0].numel() * outs[0].element_size()
 
-    def step():
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        pkv.paged_slot_mapping(dev_in["block_table"], dev_in["seq_lens"], dev_in["query_start_loc"],
-                               batch.num_tokens, batch.num_blocks, slots, status)
-        pkv.paged_kv_write(dev_in["k"], dev_in["v"], slots, buf.kv_cache, status)
-        pkv.paged_attention(dev_in["q"], buf.kv_cache, dev_in["block_table"], dev_in["seq_lens"],
-                            dev_in["query_start_loc"], batch.scale, buf.out, buf.workspace)
-        out_host.copy_(buf.out, non_blocking=True)
+    def submit(i):
+        pipe.next_inputs()
+        return pipe.submit(outs[i % 2], kv_cache=bufs[i % layers].kv_cache)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    for i in range(max(3, args.warmup)):
+        submit(i)
+    pipe.synchronize()
     if dist:
         dist.barrier()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(args.steps):
-        step()
-    e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e)
+    if scrub is not None:
+        ms = 0.0
+        for i in range(args.steps):
+            scrub_l2(scrub)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(pipe.h2d)
+            submit(i)
+            b.record(pipe.d2h)
+            pipe.synchronize()
+            ms += a.elapsed_time(b)
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(pipe.h2d)
+        for i in range(args.steps):
+            submit(i)
+        b.record(pipe.d2h)
+        pipe.synchronize()
+        ms = a.elapsed_time(b)
+    st, wst = pipe.read_status()
+    if st or wst:
+        raise RuntimeError(f"device status bits set in the host-buffer steps: {st:#x} {wst:#x}")
+    # the host copy of the output is the device step's output, bit for bit
+    last = args.steps - 1
+    if not torch.equal(outs[last % 2].view(torch.int16), bufs[last % layers].out.cpu().view(torch.int16)):
+        raise RuntimeError("host-buffer step output differs from the device step")
     ms = max_over_ranks(ms, dist, dev)
     world = dist.get_world_size() if dist else 1
     return {"value": job_tokens_per_s(world, batch.num_tokens, ms / args.steps), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+            "path": "binding.HostStepPipeline: one packed pinned-host-to-device copy of the step's inputs and one "
+                    "device-to-host copy of its output per step, overlapped with the neighbouring steps' kernels"}
 
 
 if __name__ == "__main__":

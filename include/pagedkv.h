@@ -183,6 +183,13 @@ int paged_attention_min_workspace_bytes(int32_t max_num_reqs, int32_t max_num_to
  * the same stream. Long contexts are split across CTAs (split-KV) and
  * merged with a log-sum-exp weighted reduction.
  *
+ * Ordering: block_table, seq_lens and query_start_loc must hold this call's
+ * values when the call is enqueued (written by host copies, or by kernels
+ * that complete before their dependents launch): the work-list kernel may
+ * start reading them while the stream's previous kernel is still running.
+ * q and kv_cache are read only after every earlier kernel on the stream
+ * has completed. The workspace is written only after that point too.
+ *
  *  q          bf16 [num_tokens][num_q_heads][head_size], head_size 64 or 128
  *  kv_cache   bf16 pool (read only)
  *  out        bf16 [num_tokens][num_q_heads][head_size]; rows of requests

@@ -355,6 +355,136 @@ class StepGraph:
         return self.buffers.out
 
 
+class HostStepPipeline:
+    """Steps whose inputs (q, k, v and the metadata tables) come from host
+    memory and whose output goes back to host memory.
+
+    Each step's inputs sit in one packed pinned host buffer and cross to the
+    device in ONE copy; the output returns in one copy. ``depth`` slots
+    alternate: step i+1's host-to-device copy runs on one copy stream while
+    step i computes, and step i's output returns on a second copy stream
+    while step i+1 computes. Each step is the same three calls as
+    ``StepBuffers.step`` (slot mapping, KV write, attention) on the compute
+    stream, so steps still run in order against the pool. Only the copies,
+    streams and events are PyTorch's.
+
+    Use: ``inp = pipe.next_inputs()`` (host views q, k, v, block_table,
+    seq_lens, query_start_loc of the next slot; waits until that slot's
+    previous copy has left), fill them, then ``pipe.submit(out_host)``. The
+    step's ``out_host`` is complete after ``synchronize()`` or after the
+    event ``submit`` returns.
+    """
+
+    def __init__(self, kv_cache: torch.Tensor, max_num_reqs: int, num_tokens: int, max_blocks_per_req: int,
+                 num_q_heads: int, scale: float, depth: int = 2, compute_stream=None):
+        dev = kv_cache.device
+        d = cache_desc(kv_cache)
+        self.kv_cache = kv_cache
+        self.scale = float(scale)
+        self.num_tokens = int(num_tokens)
+        self.num_blocks = int(d.num_blocks)
+        self.max_num_reqs = int(max_num_reqs)
+        self.depth = int(depth)
+        self.compute = compute_stream or torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        T, Hq, Hkv, D = self.num_tokens, int(num_q_heads), int(d.num_kv_heads), int(d.head_size)
+        R, M = self.max_num_reqs, int(max_blocks_per_req)
+        # packed layout: (name, dtype, shape), each array 256-byte aligned
+        spec = [("q", torch.bfloat16, (T, Hq, D)), ("k", torch.bfloat16, (T, Hkv, D)),
+                ("v", torch.bfloat16, (T, Hkv, D)), ("block_table", torch.int32, (R, M)),
+                ("seq_lens", torch.int32, (R,)), ("query_start_loc", torch.int32, (R + 1,))]
+        offs, off = [], 0
+        for _, dt, shp in spec:
+            n = 1
+            for x in shp:
+                n *= x
+            offs.append(off)
+            off += -(-n * torch.tensor([], dtype=dt).element_size() // 256) * 256
+        self.packed_bytes = off
+
+        def views(raw):
+            out = {}
+            for (name, dt, shp), o in zip(spec, offs):
+                n = 1
+                for x in shp:
+                    n *= x
+                size = torch.tensor([], dtype=dt).element_size()
+                out[name] = raw[o:o + n * size].view(dt).view(shp)
+            return out
+
+        self.host_raw = [torch.empty(off, dtype=torch.uint8, pin_memory=True) for _ in range(self.depth)]
+        self.dev_raw = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(self.depth)]
+        self.host_in = [views(r) for r in self.host_raw]
+        self.dev_in = [views(r) for r in self.dev_raw]
+        self.slot_mapping = [torch.empty(T, dtype=torch.int32, device=dev) for _ in range(self.depth)]
+        self.out = [torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) for _ in range(self.depth)]
+        self.loaded = [torch.cuda.Event() for _ in range(self.depth)]
+        self.computed = [torch.cuda.Event() for _ in range(self.depth)]
+        self.returned = [torch.cuda.Event() for _ in range(self.depth)]
+        self.used = [False] * self.depth
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = alloc_workspace(R, self.num_tokens, Hq, kv_cache)
+        self.i = 0
+
+    def slot_inputs(self, slot: int) -> dict:
+        """Host views of one slot, for filling every slot before the first
+        step (no waiting: call it only while no step is in flight)."""
+        return self.host_in[slot]
+
+    def next_inputs(self) -> dict:
+        """Host views to fill with the next step's inputs."""
+        b = self.i % self.depth
+        if self.used[b]:
+            self.loaded[b].synchronize()  # the slot's previous copy has been read
+        return self.host_in[b]
+
+    def submit(self, out_host: torch.Tensor, num_reqs: int | None = None, kv_cache=None) -> torch.cuda.Event:
+        """Enqueue the step whose inputs are in ``next_inputs()``; returns the
+        event after which ``out_host`` holds its output. ``num_reqs``: the
+        requests of this step (default: all). ``kv_cache``: this step's pool
+        when it is not the one the pipeline was built with (another layer's
+        pool of the same shape)."""
+        pool = self.kv_cache if kv_cache is None else kv_cache
+        if pool.shape != self.kv_cache.shape or pool.dtype != self.kv_cache.dtype:
+            raise PagedKVError(PKV_E_DIMS, "kv_cache differs in shape from the pipeline's pool")
+        R = self.max_num_reqs if num_reqs is None else int(num_reqs)
+        if not 0 < R <= self.max_num_reqs:
+            raise PagedKVError(PKV_E_DIMS, "num_reqs outside the pipeline's bounds")
+        b = self.i % self.depth
+        din = self.dev_in[b]
+        with torch.cuda.stream(self.h2d):
+            if self.used[b]:
+                self.h2d.wait_event(self.computed[b])  # the step that last read this slot is done
+            self.dev_raw[b].copy_(self.host_raw[b], non_blocking=True)
+            self.loaded[b].record(self.h2d)
+        self.compute.wait_event(self.loaded[b])
+        if self.used[b]:
+            self.compute.wait_event(self.returned[b])  # its previous output has left the device
+        bt, sl, qsl = din["block_table"][:R], din["seq_lens"][:R], din["query_start_loc"][:R + 1]
+        paged_slot_mapping(bt, sl, qsl, self.num_tokens, self.num_blocks, self.slot_mapping[b], self.status,
+                           self.compute)
+        paged_kv_write(din["k"], din["v"], self.slot_mapping[b], pool, self.status, self.compute)
+        paged_attention(din["q"], pool, bt, sl, qsl, self.scale, self.out[b], self.workspace, self.compute)
+        self.computed[b].record(self.compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[b])
+            out_host.copy_(self.out[b], non_blocking=True)
+            self.returned[b].record(self.d2h)
+        self.used[b] = True
+        self.i += 1
+        return self.returned[b]
+
+    def synchronize(self) -> None:
+        for st in (self.h2d, self.compute, self.d2h):
+            st.synchronize()
+
+    def read_status(self) -> tuple[int, int]:
+        """(slot mapping / KV write status, attention status)."""
+        self.synchronize()
+        return pkv_read_status(self.status, self.compute), pkv_read_status(self.workspace, self.compute)
+
+
 def run_step(batch, tensors: dict, stream=None) -> dict:
     """One step on device tensors; raises if a device status bit is set."""
     buf = StepBuffers(batch, tensors)

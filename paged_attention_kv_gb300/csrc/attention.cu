@@ -174,32 +174,44 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     extern __shared__ int32_t s_dyn[];
     __shared__ long long s_ll[32];
     __shared__ unsigned long long s_ull[32];
-    __shared__ int s_split, s_kvmax, s_full_total, s_full_count;
+    __shared__ int s_split, s_kvmax, s_full_total, s_full_count, s_n_items, s_n_chunk_items;
     __shared__ int s_pcap, s_pfx, s_cas_ok;  // shared-prefix pass: cap, blocks found, still possible
     __shared__ int4 s_place[kPlanThreads];  // per group of a chunk: first full-split item, first tail item, splits
     __shared__ int s_bucket_count[kSizeBuckets], s_bucket_base[kSizeBuckets], s_bucket_cursor[kSizeBuckets];
     __shared__ int s_cbucket_count[kSizeBuckets], s_cbucket_base[kSizeBuckets], s_cbucket_cursor[kSizeBuckets];
+    __shared__ int s_status;  // status bits found before the workspace may be written
     pdl_launch_dependents();
-    pdl_wait();
     const int tid = threadIdx.x;
     const int R = a.num_reqs, Hkv = a.num_kv_heads, g = a.group;
-    int32_t *status = &a.header->status;
     const int stride = R + 1;
     const bool req_smem = R <= kPlanSmemReqs;
     int32_t *cache = req_smem ? s_dyn : a.req_cache;
     int32_t *req_n = cache, *req_L = cache + stride, *req_q0 = cache + 2 * stride, *req_g = cache + 3 * stride;
     int32_t *req_c = cache + 4 * stride;  // first chunk tile of each request
     int32_t *grp_req = a.group_req, *grp_kvb = a.group_kvb;
-    if (req_smem && a.groups_cap <= kPlanSmemGroups) {
+    // With every per-request and per-group table in shared memory, steps 1-3
+    // only read this call's metadata (query_start_loc, seq_lens,
+    // block_table, complete before the call is enqueued) and write shared
+    // memory, so they overlap the previous kernel; the workspace (still read
+    // by the previous call's attention kernels) is written only after
+    // pdl_wait.
+    const bool early = req_smem && a.groups_cap <= kPlanSmemGroups;
+    if (early) {
         grp_req = s_dyn + kReqCacheArrays * stride;
         grp_kvb = grp_req + a.groups_cap;
+    } else {
+        pdl_wait();
     }
+    int32_t *status = early ? &s_status : &a.header->status;
 
     if (tid == 0) {
-        a.header->status = 0;
-        a.header->next_item = 0;
-        a.header->next_chunk_item = 0;
-        a.header->diag = 0;
+        s_status = 0;
+        if (!early) {
+            a.header->status = 0;
+            a.header->next_item = 0;
+            a.header->next_chunk_item = 0;
+            a.header->diag = 0;
+        }
         s_kvmax = 0;
         s_pcap = kCascadeMaxBlocks;
         s_cas_ok = R >= kCascadeMinReqs ? 1 : 0;
@@ -387,6 +399,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             s_cbucket_base[b] = cacc;
             cacc += s_cbucket_count[b];
         }
+        s_n_items = acc;
+        s_n_chunk_items = cacc;
+    }
+    __syncthreads();
+    if (early) {
+        pdl_wait();
+        if (tid == 0) {
+            a.header->status = s_status;
+            a.header->next_item = 0;
+            a.header->next_chunk_item = 0;
+            a.header->diag = 0;
+        }
+        status = &a.header->status;
+    }
+    if (tid == 0) {
+        const int acc = s_n_items, cacc = s_n_chunk_items;
         a.header->n_items = (int)min((long long)acc, a.items_cap);
         if (acc > a.items_cap) atomicOr(status, PKV_DEV_OVERFLOW);
         a.header->n_chunk_items = cacc;

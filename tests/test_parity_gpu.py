@@ -297,3 +297,36 @@ def test_kv_block_gather_scatter_bit_exact(shape):
     bad = torch.tensor([0, batch.num_blocks + 3, -1], dtype=torch.int32, device="cuda")
     pkv.paged_kv_gather_blocks(pool, bad, status=status)
     assert pkv.pkv_read_status(status) & pkv.PKV_DEV_BAD_BLOCK
+
+
+@pytest.mark.parametrize("workload", ["tinyllama", "mixed"])
+def test_host_step_pipeline_matches_device_steps(workload):
+    """Steps fed from pinned host memory through the double-buffered
+    pipeline (copies overlapping the neighbouring steps' kernels) return, in
+    host memory, the same bits as the same steps run on device buffers; two
+    query sets alternate so a stale buffer would show."""
+    batch = wl.make_batch(workload)
+    ten = device_tensors(batch)
+    q2 = (ten["q"].float() * -0.5).to(torch.bfloat16)
+    refs = []
+    for q in (ten["q"], q2):
+        buf = pkv.StepBuffers(batch, {**{k: v.clone() for k, v in ten.items()}, "q": q})
+        refs.append(buf.step().cpu())
+    torch.cuda.synchronize()
+    s = batch.shape
+    pipe = pkv.HostStepPipeline(ten["kv_cache"].clone(), batch.num_reqs, batch.num_tokens,
+                                batch.max_blocks_per_req, s.num_q_heads, batch.scale)
+    host = {"k": ten["k"].cpu(), "v": ten["v"].cpu(), "block_table": torch.from_numpy(batch.block_table),
+            "seq_lens": torch.from_numpy(batch.seq_lens), "query_start_loc": torch.from_numpy(batch.query_start_loc)}
+    qs = [ten["q"].cpu(), q2.cpu()]
+    outs = [torch.empty(refs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(5)]
+    for i in range(5):
+        views = pipe.next_inputs()
+        views["q"].copy_(qs[i % 2])
+        for k, v in host.items():
+            views[k].copy_(v)
+        pipe.submit(outs[i])
+    pipe.synchronize()
+    assert pipe.read_status() == (0, 0)
+    for i in range(5):
+        assert torch.equal(outs[i].view(torch.int16), refs[i % 2].view(torch.int16)), i
