@@ -40,6 +40,7 @@ UNIT = "tokens/s"
 KERNEL_SOURCES = ("attention.cu", "attention_plan.cuh", "pkv_device.cuh")
 PROFILE_DOC = os.path.join(REPO, "profiles", "attention_decode_kernel_llama8b.md")
 KERNEL_SOURCES_CHUNK = ("attention_chunk.cu", "attention_chunk.h", "attention_plan.cuh", "pkv_device.cuh")
+PROFILE_DOC_CHUNK = os.path.join(REPO, "profiles", "chunk_kernel_mixed.md")
 
 
 def launches_per_step(batch) -> int:
@@ -176,24 +177,24 @@ def algorithmic_bytes(batch, only=None) -> dict:
             "attention_total": kv + qo + bt + meta, "unique_tokens": unique_tokens}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(REPO, "paged_attention_kv_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic():
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+def profiled_traffic(doc=PROFILE_DOC, sources=KERNEL_SOURCES):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
     try:
-        text = open(PROFILE_DOC).read()
+        text = open(doc).read()
     except OSError:
         return None
     src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not val or src.group(1) != kernel_source_hash():
+    if not src or not val or src.group(1) != kernel_source_hash(sources):
         return None
     return float(val.group(1))
 
@@ -214,7 +215,8 @@ def chunk_roofline(batch, chunk_ms: float, peaks: dict) -> dict:
     return {"bound": "tensor", "kernel": "chunk_kernel (tcgen05)", "achieved": achieved,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
             "peak_source": f"{peaks['source']} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-            "flops_per_launch": fl, "kernel_us": chunk_ms * 1e3, "traffic": None}
+            "flops_per_launch": fl, "kernel_us": chunk_ms * 1e3,
+            "traffic": profiled_traffic(PROFILE_DOC_CHUNK, KERNEL_SOURCES_CHUNK) if batch.workload == "mixed" else None}
 
 
 # --------------------------------------------------------------------------

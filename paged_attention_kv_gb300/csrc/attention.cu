@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
                 ok = true;
                 const long long rows = (long long)n * g;
                 if (a.chunk_ok && rows >= kChunkRows) {
-                    tiles = (unsigned long long)((rows + kChunkRows - 1) / kChunkRows) << 32;
+                    tiles = (unsigned long long)((rows + kChunkPairRows - 1) / kChunkPairRows) << 32;
                     atomicMax(&s_kvmax, L);
                     s_cas_ok = 0;  // the shared-prefix pass covers split-KV rows only
                 } else {
@@ -322,8 +322,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0 && P0 > 0)  // the prefix tiles
         work += ((long long)a.num_tokens * g + kRowsPerTile - 1) / kRowsPerTile * Hkv * P0;
     const int kvmax = s_kvmax;
-    auto chunk_kv_end = [&](int r, int mt) {
-        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
+    auto chunk_kv_end = [&](int r, int pair) {  // keys seen by the pair's last row
+        const long long last_row =
+            min((long long)req_n[r] * g - 1, (long long)pair * kChunkPairRows + kChunkPairRows - 1);
         return req_L[r] - req_n[r] + (int)(last_row / g) + 1;
     };
     auto chunk_bucket = [&](int kv_end) {  // longest first
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         if (gi >= n_cgroups) continue;
         const int n = req_n[r];
         const long long rows = (long long)n * g;
-        const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
+        const int nv = (int)min((long long)kChunkPairRows, rows - (long long)mt * kChunkPairRows);
         for (int h = 0; h < Hkv; ++h) {
             const int idx = first + h;
             ChunkItem c;

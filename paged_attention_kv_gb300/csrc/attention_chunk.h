@@ -11,7 +11,8 @@
 
 namespace pkv {
 
-// a = {r, row tile mt (128 rows), kv head h, kv_end}, b = {qstart, n, L, valid rows}.
+// a = {r, tile pair (256 rows), kv head h, keys seen by the pair's last row},
+// b = {qstart, n, L, valid rows of the pair}.
 struct ChunkItem {
     int4 a, b;
 };

@@ -56,8 +56,11 @@ constexpr int kCascadeMinReqs = 4;
 constexpr int kCascadeMaxBlocks = 4096;
 
 // Chunk tiles (tcgen05 path): requests with at least kChunkRows query rows
-// (n * g) are cut into 128-row tiles that run over 128-key tiles.
+// (n * g) are cut into 128-row tiles that run over 128-key tiles; one work
+// item takes two consecutive tiles of a request (kChunkPairRows rows), which
+// share one K/V stream.
 constexpr int kChunkRows = 128;
+constexpr int kChunkPairRows = 2 * kChunkRows;
 constexpr int kChunkKeys = 128;
 
 struct WsHeader {
