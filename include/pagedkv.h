@@ -154,9 +154,12 @@ int paged_kv_scatter_blocks(const void *staging, const int32_t *block_ids, int32
 /*
  * Workspace bytes paged_attention needs for batches of at most
  * max_num_reqs requests and max_num_tokens new tokens on the current
- * device. A smaller workspace (down to the size for max_num_reqs and
- * max_num_tokens with no room for split-KV partials) still works: the
- * library then splits long contexts less, or not at all.
+ * device. It includes split-KV partial rows for the persistent grid and,
+ * up to 2^20 rows, two per query row (room for the shared-prefix pass). A
+ * smaller workspace (down to the size for max_num_reqs and max_num_tokens
+ * with no room for split-KV partials) still works: the library then splits
+ * long contexts less, or not at all, and skips the shared-prefix pass when
+ * its partial rows do not fit.
  */
 int paged_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens, int32_t num_q_heads,
                                     const pkv_cache_desc *desc, size_t *bytes);

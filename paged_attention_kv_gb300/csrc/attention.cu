@@ -1117,8 +1117,13 @@ int device_info(DeviceInfo **out) {
 
 // Default split-KV partial capacity in rows: twice a full persistent grid's
 // worth of split items (up to 3 CTAs per SM), each with a full 16-row tile.
-long long default_part_rows_cap(int sm_count) {
-    return (long long)sm_count * 3 * kItemsPerCta * kRowsPerTile * 2;
+// Partial-row capacity a full workspace gets: enough for the split-KV
+// schedule of a persistent grid, and for two slots per query row (a shared-
+// prefix slot and one split) up to 2^20 rows.
+long long default_part_rows_cap(int sm_count, long long num_tokens, int num_q_heads) {
+    const long long grid_rows = (long long)sm_count * 3 * kItemsPerCta * kRowsPerTile * 2;
+    const long long prefix_rows = min(2 * num_tokens * num_q_heads, 1LL << 20);
+    return max(grid_rows, prefix_rows);
 }
 
 int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &d) {
@@ -1175,12 +1180,15 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     rc = device_info(&di);
     if (rc) return rc;
     // Largest partial capacity (up to the default) that fits the workspace.
-    long long part_rows = default_part_rows_cap(di->sm_count);
-    const size_t spare = workspace_bytes - base.total;
-    const long long fit = spare > 1024 ? (long long)((spare - 1024) / part_row_bytes(D)) : 0;
-    if (fit < part_rows) part_rows = fit;
-    const WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, Hkv, D, part_rows);
-    if (L.total > workspace_bytes) return PKV_E_WORKSPACE;
+    long long part_rows = default_part_rows_cap(di->sm_count, num_tokens, num_q_heads);
+    WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, Hkv, D, part_rows);
+    if (L.total > workspace_bytes) {
+        const size_t spare = workspace_bytes - base.total;
+        const long long fit = spare > 1024 ? (long long)((spare - 1024) / part_row_bytes(D)) : 0;
+        if (fit < part_rows) part_rows = fit;
+        L = ws_layout(num_reqs, num_tokens, num_q_heads, Hkv, D, part_rows);
+        if (L.total > workspace_bytes) return PKV_E_WORKSPACE;
+    }
 
     CUtensorMap kv_map;
     rc = encode_kv_map(&kv_map, kv_cache, *desc);
@@ -1294,7 +1302,7 @@ extern "C" PKV_API int paged_attention_workspace_bytes(int32_t max_num_reqs, int
     rc = device_info(&di);
     if (rc) return rc;
     const WsLayout L = ws_layout(max_num_reqs, max_num_tokens, num_q_heads, desc->num_kv_heads, desc->head_size,
-                                 default_part_rows_cap(di->sm_count));
+                                 default_part_rows_cap(di->sm_count, max_num_tokens, num_q_heads));
     *bytes = L.total;
     return PKV_OK;
 }

@@ -60,14 +60,14 @@ def test_more_requests_than_the_shared_memory_tables():
 
 
 def test_more_requests_than_the_tables_with_a_shared_prefix():
-    """4500 decode requests sharing 4 blocks: the prefix tiles would need a
-    second partial slot for every row, more than the workspace's partial
-    capacity, so the work-list kernel drops them; the outputs still match."""
+    """4500 decode requests sharing 4 blocks: the prefix tiles run from the
+    workspace-table path too (the full workspace holds two partial slots per
+    query row)."""
     rng = np.random.default_rng(511)
     seq = 64 + rng.integers(1, 150, size=4500)
     batch = wl.custom_batch(LLAMA, seq, np.ones(4500, np.int64), 512, shared_prefix_blocks=4)
     buf = _check_sampled(batch, _rows(batch, 3000, 513, extra_tokens=(0, 4499)))
-    assert _record(buf)["cascade_blocks"] == 0
+    assert _record(buf)["cascade_blocks"] == 4
 
 
 def test_more_query_rows_than_the_shared_memory_group_tables():
