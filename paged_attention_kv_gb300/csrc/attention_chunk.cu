@@ -141,16 +141,18 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
         mbar_init(drain, 1);
         mbar_fence_init();
     }
+    // The barrier setup above overlaps the previous kernel; the work list it
+    // wrote is read only after this. A batch without chunk tiles ends here,
+    // before any TMEM is allocated.
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n_items = a.header->n_chunk_items;
+    if (n_items == 0) return;
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tm = *tmem_slot;
-    // The prologue above overlaps the previous kernel; the work list it
-    // wrote is read only after this.
-    pdl_wait();
-    pdl_launch_dependents();
-    const int n_items = a.header->n_chunk_items;
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
