@@ -38,7 +38,16 @@
 namespace pkv {
 namespace {
 
-constexpr int kChunkThreads = 320;
+// Warps 0-3 softmax of tile A, 4-7 of tile B (one warpgroup each), 8 TMA
+// producer, 9 MMA issuer, 10-11 idle (they only give their registers to
+// the softmax warpgroups).
+constexpr int kChunkThreads = 384;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// Register budget per thread after the split (launch allocation: 168 per
+// thread at 384 threads). 256 softmax threads x 192 + 128 x 120 = 64512 =
+// 384 x 168: the decreases return exactly what the increases take; per
+// sub-partition 192 + 192 + 120 = 504 <= 512.
+constexpr uint32_t kRegsSoftmax = 192, kRegsOther = 120;
 constexpr uint32_t kTmemCols = 512;       // S_A | S_B | O_A | O_B
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8
 constexpr int kSoftmaxArrivals = 4;       // warps per tile
@@ -148,212 +157,216 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     pdl_launch_dependents();
     const int n_items = a.header->n_chunk_items;
     if (n_items == 0) return;
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tm = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            tma_prefetch_desc(&kv_map);
-            tma_prefetch_desc(&q_map);
-        }
-        const int Hkv = a.num_kv_heads;
-        uint32_t jt = 0;                   // K/V tiles of the items so far
-        uint32_t k_issued = 0, v_issued = 0;
-        bool ok = true;
-        for (int k = 0; ok; ++k) {
-            int it = 0;
-            if (lane == 0) it = atomicAdd(&a.header->next_chunk_item, 1);
-            it = __shfl_sync(0xffffffffu, it, 0);
-            if (!mbar_wait(q_taken, (k & 1) ^ 1, status, abort) || !mbar_wait(q_empty, (k & 1) ^ 1, status, abort)) {
-                ok = false;
-                break;
-            }
-            if (it >= n_items) {
-                if (lane == 0) {
-                    desc->item = -1;
-                    mbar_arrive(q_full);
-                }
-                break;
-            }
-            const ChunkItem w = a.items[it];
-            const int r = w.a.x, pair = w.a.y, h = w.a.z;
-            const int q0 = w.b.x, n = w.b.y, L = w.b.z, nv = w.b.w;  // nv: valid rows of the pair
-            const int nv_a = min(kChunkRows, nv), nv_b = nv - nv_a;
-            const int row0 = pair * kChunkPairRows;
-            const int kv_end_a = chunk_tile_kv_end(n, L, g, row0, nv_a);
-            const int kv_end_b = nv_b > 0 ? chunk_tile_kv_end(n, L, g, row0 + kChunkRows, nv_b) : 0;
-            const int nt_a = (kv_end_a + kChunkKeys - 1) / kChunkKeys;
-            const int nt_b = (kv_end_b + kChunkKeys - 1) / kChunkKeys;
-            const int nt = max(nt_a, nt_b);
-            const int kvb = (max(kv_end_a, kv_end_b) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    if (warp >= 2 * kSoftmaxArrivals) {
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == kProducerWarp) {
+            // ------------------------------ producer ------------------------------
             if (lane == 0) {
-                ChunkDesc d;
-                d.item = it; d.r = r; d.pair = pair; d.h = h; d.q0 = q0; d.n = n; d.L = L;
-                d.nv_a = nv_a; d.nv_b = nv_b; d.kv_end_a = kv_end_a; d.kv_end_b = kv_end_b;
-                d.nt_a = nt_a; d.nt_b = nt_b;
-                *desc = d;
-                const int tiles = nv_b > 0 ? 2 : 1;
-                mbar_arrive_expect_tx(q_full, (uint32_t)tiles * kChunkRows * D * 2);
-                for (int t = 0; t < tiles; ++t) {
-                    const int tok = q0 + (row0 + t * kChunkRows) / g;
-#pragma unroll
-                    for (int bx = 0; bx < D / 64; ++bx)
-                        tma_load_3d(smem + S::kOffQ + t * S::kTile + bx * S::kHalf, &q_map, bx * 64, h * g, tok,
-                                    q_full);
-                }
+                tma_prefetch_desc(&kv_map);
+                tma_prefetch_desc(&q_map);
             }
-            __syncwarp();
-            const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
-            // K or V of key tile j into its ring slot: eight blocks, one box
-            // per 64 columns of each.
-            auto load = [&](bool is_v, int j) {
-                const uint32_t x = jt + j;
-                const int st = x % kStages;
-                uint64_t *full = is_v ? &v_full[st] : &k_full[st];
-                if (!mbar_wait(is_v ? &v_empty[st] : &k_empty[st], ((x / kStages) & 1) ^ 1, status, abort))
-                    return false;
-                int blk = a.num_blocks;  // past the map: TMA fills zeros
-                const int kb = j * (kChunkKeys / PKV_BLOCK_SIZE) + lane;
-                if (lane < kChunkKeys / PKV_BLOCK_SIZE && kb < kvb) {
-                    blk = __ldg(bt + kb);
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        raise_status(status, PKV_DEV_BAD_BLOCK);
-                        blk = a.num_blocks;
-                    }
-                }
-                if (lane == 0) mbar_arrive_expect_tx(full, kChunkKeys * D * 2);
-                __syncwarp();
-                if (lane < kChunkKeys / PKV_BLOCK_SIZE) {
-                    uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * 2048;
-                    const int row = (is_v ? Hkv + h : h) * PKV_BLOCK_SIZE;
-#pragma unroll
-                    for (int bx = 0; bx < D / 64; ++bx) tma_load_3d(dst + bx * S::kHalf, &kv_map, bx * 64, row, blk, full);
-                }
-                __syncwarp();
-                if (is_v) ++v_issued; else ++k_issued;
-                return true;
-            };
-            // K runs one tile ahead of V.
-            ok = load(false, 0);
-            for (int j = 0; j < nt && ok; ++j) {
-                if (j + 1 < nt) ok = load(false, j + 1);
-                if (ok) ok = load(true, j);
-            }
-            jt += nt;
-        }
-        if (!ok && lane == 0) {
-            // let copies already issued land before the CTA can leave
-            for (uint32_t x = k_issued > (uint32_t)kStages ? k_issued - kStages : 0; x < k_issued; ++x)
-                mbar_drain(&k_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
-            for (uint32_t x = v_issued > (uint32_t)kStages ? v_issued - kStages : 0; x < v_issued; ++x)
-                mbar_drain(&v_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
-        }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer -----------------------------
-        // The whole warp runs this loop with the same values (so descriptors
-        // and TMEM addresses stay warp-uniform); one elected lane issues
-        // every tcgen05.mma and commit.
-        {
-            constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys, 0, 0);
-            constexpr uint32_t kIdPV = umma_idesc_bf16(128, D, 0, 1);
-            const uint32_t q_s = smem_u32(smem + S::kOffQ);
-            const uint32_t k_s = smem_u32(smem + S::kOffK), v_s = smem_u32(smem + S::kOffV);
-            uint32_t jt = 0;                 // K/V tiles consumed so far
-            uint32_t n_p[2] = {0, 0};        // P handoffs taken per tile
-            uint32_t n_items_t[2] = {0, 0};  // items finished per tile
+            const int Hkv = a.num_kv_heads;
+            uint32_t jt = 0;                   // K/V tiles of the items so far
+            uint32_t k_issued = 0, v_issued = 0;
             bool ok = true;
-            // S_t(x) = Q_t K(x)^T into TMEM columns t * 128
-            auto issue_s = [&](int t, uint32_t x) {
-                const int st = x % kStages;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * S::kHalf + (kk % 4) * 32;
-                    umma_bf16_warp(tm + t * kChunkKeys, umma_desc_sw128(q_s + t * S::kTile + off, 16, 1024),
-                                   umma_desc_sw128(k_s + st * S::kTile + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit_warp(&s_full[t]);
-            };
             for (int k = 0; ok; ++k) {
-                if (!warp_wait(q_full, k & 1, status, abort)) { ok = false; break; }
-                const ChunkDesc d = *desc;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(q_taken);
-                if (d.item < 0) break;
-                const int nt_t[2] = {d.nt_a, d.nt_b};
-                const int nt = max(d.nt_a, d.nt_b);
-                int s_left = d.nt_a + d.nt_b;  // S products of this item still to issue
-                // S of the first key tile, for both tiles
-                if (!warp_wait(&k_full[jt % kStages], (jt / kStages) & 1, status, abort)) { ok = false; break; }
-                tmem_fence_after_sync();
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (nt_t[t] > 0) {
-                        issue_s(t, jt);
-                        if (--s_left == 0) umma_commit_warp(q_empty);
+                int it = 0;
+                if (lane == 0) it = atomicAdd(&a.header->next_chunk_item, 1);
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (!mbar_wait(q_taken, (k & 1) ^ 1, status, abort) || !mbar_wait(q_empty, (k & 1) ^ 1, status, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (it >= n_items) {
+                    if (lane == 0) {
+                        desc->item = -1;
+                        mbar_arrive(q_full);
+                    }
+                    break;
+                }
+                const ChunkItem w = a.items[it];
+                const int r = w.a.x, pair = w.a.y, h = w.a.z;
+                const int q0 = w.b.x, n = w.b.y, L = w.b.z, nv = w.b.w;  // nv: valid rows of the pair
+                const int nv_a = min(kChunkRows, nv), nv_b = nv - nv_a;
+                const int row0 = pair * kChunkPairRows;
+                const int kv_end_a = chunk_tile_kv_end(n, L, g, row0, nv_a);
+                const int kv_end_b = nv_b > 0 ? chunk_tile_kv_end(n, L, g, row0 + kChunkRows, nv_b) : 0;
+                const int nt_a = (kv_end_a + kChunkKeys - 1) / kChunkKeys;
+                const int nt_b = (kv_end_b + kChunkKeys - 1) / kChunkKeys;
+                const int nt = max(nt_a, nt_b);
+                const int kvb = (max(kv_end_a, kv_end_b) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+                if (lane == 0) {
+                    ChunkDesc d;
+                    d.item = it; d.r = r; d.pair = pair; d.h = h; d.q0 = q0; d.n = n; d.L = L;
+                    d.nv_a = nv_a; d.nv_b = nv_b; d.kv_end_a = kv_end_a; d.kv_end_b = kv_end_b;
+                    d.nt_a = nt_a; d.nt_b = nt_b;
+                    *desc = d;
+                    const int tiles = nv_b > 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(q_full, (uint32_t)tiles * kChunkRows * D * 2);
+                    for (int t = 0; t < tiles; ++t) {
+                        const int tok = q0 + (row0 + t * kChunkRows) / g;
+    #pragma unroll
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_load_3d(smem + S::kOffQ + t * S::kTile + bx * S::kHalf, &q_map, bx * 64, h * g, tok,
+                                        q_full);
                     }
                 }
-                umma_commit_warp(&k_empty[jt % kStages]);  // both S products of key tile 0 are issued
-                for (int j = 0; j < nt && ok; ++j) {
+                __syncwarp();
+                const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
+                // K or V of key tile j into its ring slot: eight blocks, one box
+                // per 64 columns of each.
+                auto load = [&](bool is_v, int j) {
                     const uint32_t x = jt + j;
                     const int st = x % kStages;
-                    bool v_ready = false, k_next_ready = false;
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (j >= nt_t[t]) continue;
-                        if (!warp_wait(&p_full[t], n_p[t] & 1, status, abort)) { ok = false; break; }
-                        ++n_p[t];
-                        if (j == 0 && n_items_t[t] > 0 &&
-                            !warp_wait(&o_free[t], (n_items_t[t] - 1) & 1, status, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        if (!v_ready) {
-                            if (!warp_wait(&v_full[st], (x / kStages) & 1, status, abort)) { ok = false; break; }
-                            v_ready = true;
-                        }
-                        tmem_fence_after_sync();
-                        // O_t += P_t V: P_t from TMEM (64 columns of bf16 pairs), V MN-major.
-#pragma unroll
-                        for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
-                            const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + kk * 2048, S::kHalf, 1024);
-                            umma_bf16_tmem_a_warp(tm + 256 + t * D, tm + t * kChunkKeys + kk * 8, bd, kIdPV,
-                                                  (j > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        if (j == nt_t[t] - 1) {
-                            umma_commit_warp(&o_done[t]);
-                            ++n_items_t[t];
-                        }
-                        if (t == 1 || nt_t[1] <= j) umma_commit_warp(&v_empty[st]);  // last PV on this V tile
-                        if (j + 1 < nt_t[t]) {
-                            // S_t(j+1) follows PV_t(j), which read P_t from the same columns
-                            if (!k_next_ready) {
-                                const uint32_t y = x + 1;
-                                if (!warp_wait(&k_full[y % kStages], (y / kStages) & 1, status, abort)) {
-                                    ok = false;
-                                    break;
-                                }
-                                k_next_ready = true;
-                            }
-                            issue_s(t, x + 1);
-                            if (--s_left == 0) umma_commit_warp(q_empty);
-                            if (t == 1 || nt_t[1] <= j + 1) umma_commit_warp(&k_empty[(x + 1) % kStages]);
+                    uint64_t *full = is_v ? &v_full[st] : &k_full[st];
+                    if (!mbar_wait(is_v ? &v_empty[st] : &k_empty[st], ((x / kStages) & 1) ^ 1, status, abort))
+                        return false;
+                    int blk = a.num_blocks;  // past the map: TMA fills zeros
+                    const int kb = j * (kChunkKeys / PKV_BLOCK_SIZE) + lane;
+                    if (lane < kChunkKeys / PKV_BLOCK_SIZE && kb < kvb) {
+                        blk = __ldg(bt + kb);
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            raise_status(status, PKV_DEV_BAD_BLOCK);
+                            blk = a.num_blocks;
                         }
                     }
+                    if (lane == 0) mbar_arrive_expect_tx(full, kChunkKeys * D * 2);
+                    __syncwarp();
+                    if (lane < kChunkKeys / PKV_BLOCK_SIZE) {
+                        uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * 2048;
+                        const int row = (is_v ? Hkv + h : h) * PKV_BLOCK_SIZE;
+    #pragma unroll
+                        for (int bx = 0; bx < D / 64; ++bx) tma_load_3d(dst + bx * S::kHalf, &kv_map, bx * 64, row, blk, full);
+                    }
+                    __syncwarp();
+                    if (is_v) ++v_issued; else ++k_issued;
+                    return true;
+                };
+                // K runs one tile ahead of V.
+                ok = load(false, 0);
+                for (int j = 0; j < nt && ok; ++j) {
+                    if (j + 1 < nt) ok = load(false, j + 1);
+                    if (ok) ok = load(true, j);
                 }
                 jt += nt;
             }
-            // make sure no MMA is still writing TMEM before it is freed
-            umma_commit_warp(drain);
-            if (lane == 0) mbar_drain(drain, 0, status, diag, 0x4);
+            if (!ok && lane == 0) {
+                // let copies already issued land before the CTA can leave
+                for (uint32_t x = k_issued > (uint32_t)kStages ? k_issued - kStages : 0; x < k_issued; ++x)
+                    mbar_drain(&k_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
+                for (uint32_t x = v_issued > (uint32_t)kStages ? v_issued - kStages : 0; x < v_issued; ++x)
+                    mbar_drain(&v_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------ MMA issuer -----------------------------
+            // The whole warp runs this loop with the same values (so descriptors
+            // and TMEM addresses stay warp-uniform); one elected lane issues
+            // every tcgen05.mma and commit.
+            {
+                constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys, 0, 0);
+                constexpr uint32_t kIdPV = umma_idesc_bf16(128, D, 0, 1);
+                const uint32_t q_s = smem_u32(smem + S::kOffQ);
+                const uint32_t k_s = smem_u32(smem + S::kOffK), v_s = smem_u32(smem + S::kOffV);
+                uint32_t jt = 0;                 // K/V tiles consumed so far
+                uint32_t n_p[2] = {0, 0};        // P handoffs taken per tile
+                uint32_t n_items_t[2] = {0, 0};  // items finished per tile
+                bool ok = true;
+                // S_t(x) = Q_t K(x)^T into TMEM columns t * 128
+                auto issue_s = [&](int t, uint32_t x) {
+                    const int st = x % kStages;
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * S::kHalf + (kk % 4) * 32;
+                        umma_bf16_warp(tm + t * kChunkKeys, umma_desc_sw128(q_s + t * S::kTile + off, 16, 1024),
+                                       umma_desc_sw128(k_s + st * S::kTile + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit_warp(&s_full[t]);
+                };
+                for (int k = 0; ok; ++k) {
+                    if (!warp_wait(q_full, k & 1, status, abort)) { ok = false; break; }
+                    const ChunkDesc d = *desc;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(q_taken);
+                    if (d.item < 0) break;
+                    const int nt_t[2] = {d.nt_a, d.nt_b};
+                    const int nt = max(d.nt_a, d.nt_b);
+                    int s_left = d.nt_a + d.nt_b;  // S products of this item still to issue
+                    // S of the first key tile, for both tiles
+                    if (!warp_wait(&k_full[jt % kStages], (jt / kStages) & 1, status, abort)) { ok = false; break; }
+                    tmem_fence_after_sync();
+    #pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (nt_t[t] > 0) {
+                            issue_s(t, jt);
+                            if (--s_left == 0) umma_commit_warp(q_empty);
+                        }
+                    }
+                    umma_commit_warp(&k_empty[jt % kStages]);  // both S products of key tile 0 are issued
+                    for (int j = 0; j < nt && ok; ++j) {
+                        const uint32_t x = jt + j;
+                        const int st = x % kStages;
+                        bool v_ready = false, k_next_ready = false;
+    #pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (j >= nt_t[t]) continue;
+                            if (!warp_wait(&p_full[t], n_p[t] & 1, status, abort)) { ok = false; break; }
+                            ++n_p[t];
+                            if (j == 0 && n_items_t[t] > 0 &&
+                                !warp_wait(&o_free[t], (n_items_t[t] - 1) & 1, status, abort)) {
+                                ok = false;
+                                break;
+                            }
+                            if (!v_ready) {
+                                if (!warp_wait(&v_full[st], (x / kStages) & 1, status, abort)) { ok = false; break; }
+                                v_ready = true;
+                            }
+                            tmem_fence_after_sync();
+                            // O_t += P_t V: P_t from TMEM (64 columns of bf16 pairs), V MN-major.
+    #pragma unroll
+                            for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
+                                const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + kk * 2048, S::kHalf, 1024);
+                                umma_bf16_tmem_a_warp(tm + 256 + t * D, tm + t * kChunkKeys + kk * 8, bd, kIdPV,
+                                                      (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            if (j == nt_t[t] - 1) {
+                                umma_commit_warp(&o_done[t]);
+                                ++n_items_t[t];
+                            }
+                            if (t == 1 || nt_t[1] <= j) umma_commit_warp(&v_empty[st]);  // last PV on this V tile
+                            if (j + 1 < nt_t[t]) {
+                                // S_t(j+1) follows PV_t(j), which read P_t from the same columns
+                                if (!k_next_ready) {
+                                    const uint32_t y = x + 1;
+                                    if (!warp_wait(&k_full[y % kStages], (y / kStages) & 1, status, abort)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    k_next_ready = true;
+                                }
+                                issue_s(t, x + 1);
+                                if (--s_left == 0) umma_commit_warp(q_empty);
+                                if (t == 1 || nt_t[1] <= j + 1) umma_commit_warp(&k_empty[(x + 1) % kStages]);
+                            }
+                        }
+                    }
+                    jt += nt;
+                }
+                // make sure no MMA is still writing TMEM before it is freed
+                umma_commit_warp(drain);
+                if (lane == 0) mbar_drain(drain, 0, status, diag, 0x4);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // --------------------------- softmax and output ---------------------------
-        const int t = (warp - 2) >> 2;  // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
+        const int t = warp >> 2;         // 0: tile A (warps 0-3), 1: tile B (warps 4-7)
         const int q4 = warp & 3;        // TMEM lane quadrant this warp may access
         const int row = q4 * 32 + lane; // query row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -394,31 +407,31 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 // ones) take a path without per-key tests; with a positive
                 // scale the max can be taken on the raw scores.
                 const bool fast = __all_sync(0xffffffffu, key0 + kChunkKeys - 1 <= limit) && a.scale_log2 > 0.f;
-                // Pass 1: the row max of this key tile (scaled, masked), 64
-                // columns per TMEM round, eight independent maxima.
+                // The row's 128 scores of this key tile: one TMEM round trip.
+                float sv[kChunkKeys / 32][32];
+#pragma unroll
+                for (int c = 0; c < kChunkKeys / 32; ++c) tmem_ld32(s_col + c * 32, sv[c]);
+#pragma unroll
+                for (int c = 0; c < kChunkKeys / 32; ++c) tmem_wait_ld_regs(sv[c]);
+                // Row max (scaled, masked), eight independent maxima.
                 float mx = -INFINITY;
                 {
                     float mxa[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) mxa[e] = -INFINITY;
+                    if (fast) {
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        float v0[32], v1[32];
-                        tmem_ld32(s_col + c2 * 64, v0);
-                        tmem_ld32(s_col + c2 * 64 + 32, v1);
-                        tmem_wait_ld_regs(v0);
-                        tmem_wait_ld_regs(v1);
-                        if (fast) {
+                        for (int c = 0; c < kChunkKeys / 32; ++c)
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) mxa[e & 7] = fmax3(mxa[e & 7], v0[e], v1[e]);
-                        } else {
+                            for (int e = 0; e < 16; ++e)
+                                mxa[(c * 16 + e) & 7] = fmax3(mxa[(c * 16 + e) & 7], sv[c][2 * e], sv[c][2 * e + 1]);
+                    } else {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int k0 = key0 + c2 * 64 + e;
-                                mxa[e & 7] = fmaxf(mxa[e & 7], k0 <= limit ? v0[e] * a.scale_log2 : -INFINITY);
-                                mxa[e & 7] = fmaxf(mxa[e & 7], k0 + 32 <= limit ? v1[e] * a.scale_log2 : -INFINITY);
-                            }
-                        }
+                        for (int c = 0; c < kChunkKeys / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                mxa[e & 7] = fmaxf(mxa[e & 7], key0 + c * 32 + e <= limit ? sv[c][e] * a.scale_log2
+                                                                                         : -INFINITY);
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) mx = fmaxf(mx, mxa[e]);
@@ -432,7 +445,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                     const bool resc = mx > m_run + kRescaleThreshold;
                     if (__any_sync(0xffffffffu, resc)) {
                         const float alpha = resc ? fast_exp2(m_run - mx) : 1.f;
-#pragma unroll
+#pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             float o[32];
                             tmem_ld32(o_col + c * 32, o);
@@ -445,26 +458,20 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                         if (resc) m_run = mx;
                     }
                 }
-                // Pass 2: P = 2^(s * scale - m_run) as bf16 pairs, written
-                // over S columns already read (32 keys -> 16 columns); the
-                // next 32 columns load while this round computes.
+                // P = 2^(s * scale - m_run) as bf16 pairs over the first 64
+                // columns of S_t (32 keys -> 16 columns per store).
                 {
                     const float neg_m = -m_run;
                     float la[4] = {0.f, 0.f, 0.f, 0.f};
                     float2 la2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                    float v[32];
-                    tmem_ld32(s_col, v);
-                    tmem_wait_ld_regs(v);
 #pragma unroll
                     for (int c = 0; c < kChunkKeys / 32; ++c) {
-                        float w[32];
-                        if (c + 1 < kChunkKeys / 32) tmem_ld32(s_col + (c + 1) * 32, w);
                         uint32_t pk[16];
                         if (fast) {
                             const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
-                                const float2 x = ffma2(make_float2(v[2 * e], v[2 * e + 1]), sc2, nm2);
+                                const float2 x = ffma2(make_float2(sv[c][2 * e], sv[c][2 * e + 1]), sc2, nm2);
                                 const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                                 la2[e & 1] = fadd2(la2[e & 1], p);
                                 pk[e] = pack_bf16x2(p.x, p.y);
@@ -473,18 +480,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int kk = key0 + c * 32 + 2 * e;
-                                const float p0 = kk <= limit ? fast_exp2(fmaf(v[2 * e], a.scale_log2, neg_m)) : 0.f;
-                                const float p1 = kk + 1 <= limit ? fast_exp2(fmaf(v[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
+                                const float p0 = kk <= limit ? fast_exp2(fmaf(sv[c][2 * e], a.scale_log2, neg_m)) : 0.f;
+                                const float p1 =
+                                    kk + 1 <= limit ? fast_exp2(fmaf(sv[c][2 * e + 1], a.scale_log2, neg_m)) : 0.f;
                                 la[e & 3] += p0 + p1;
                                 pk[e] = pack_bf16x2(p0, p1);
                             }
                         }
                         tmem_st16u(s_col + c * 16, pk);
-                        if (c + 1 < kChunkKeys / 32) {
-                            tmem_wait_ld_regs(w);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) v[e] = w[e];
-                        }
                     }
                     l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la2[0].x + la2[0].y) + (la2[1].x + la2[1].y));
                 }
@@ -548,7 +551,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
-    if (warp == 1) tmem_dealloc(tm, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tm, kTmemCols);
 }
 
 }  // namespace
