@@ -330,3 +330,17 @@ def test_host_step_pipeline_matches_device_steps(workload):
     assert pipe.read_status() == (0, 0)
     for i in range(5):
         assert torch.equal(outs[i].view(torch.int16), refs[i % 2].view(torch.int16)), i
+
+
+@pytest.mark.parametrize("shape", [TINY, LLAMA], ids=["d64", "d128"])
+def test_chunk_pairs_with_and_without_a_second_tile(shape):
+    """Chunk work items hold two 128-row tiles of a request; a request whose
+    rows end on an odd tile leaves the last item with tile A only, and a
+    pair whose tiles see different numbers of 128-key tiles shares one K/V
+    stream."""
+    g = shape.num_q_heads // shape.num_kv_heads
+    t = 128 // g  # tokens per 128-row tile
+    ql = [t, 3 * t, 5 * t, 2 * t, 1]
+    seq = [t, 3 * t + 700, 5 * t + 45, 2 * t + 128, 900]
+    batch = _custom(shape, seq, ql, 600 + g)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
