@@ -258,6 +258,17 @@ int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_head
                            float scale, void *out, void *stream);
 
 /*
+ * Failure-detection self-test: runs one thread that waits, with the bounded
+ * wait every pipeline stage of the attention kernels uses, on an mbarrier
+ * that nothing arrives on. After timeout_us (1 .. 1000000) the wait gives
+ * up, PKV_DEV_TIMEOUT is ORed into *status (device, 4-byte aligned, not
+ * cleared by the call) and the kernel returns; the CUDA context stays
+ * usable. A stuck stage in a real launch is reported the same way, after
+ * 2 s. Returns PKV_E_* for bad arguments or a launch error.
+ */
+int pkv_selftest_bounded_wait(int32_t *status, uint32_t timeout_us, void *stream);
+
+/*
  * Copies a device status word to *host_status after the work queued on
  * `stream` so far has finished (synchronises the stream). Returns PKV_OK if
  * the word is 0, PKV_E_DEVICE if bits are set, PKV_E_CUDA on a CUDA error.

@@ -40,7 +40,7 @@ PKV_DEV_OVERFLOW = 0x20
 EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_gather_blocks",
             "paged_kv_scatter_blocks", "paged_attention_workspace_bytes",
             "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
-            "paged_attention_static", "pkv_read_status", "pkv_status_string")
+            "paged_attention_static", "pkv_read_status", "pkv_selftest_bounded_wait", "pkv_status_string")
 
 
 class PagedKVError(RuntimeError):
@@ -70,6 +70,7 @@ def _load():
     lib.paged_attention.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.paged_attention_timed.argtypes = lib.paged_attention.argtypes + [ctypes.POINTER(vp)]
     lib.paged_attention_static.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp]
+    lib.pkv_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
     lib.pkv_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -289,6 +290,13 @@ def _event_handle(ev, stream) -> int:
     if not ev.cuda_event:
         ev.record(stream if stream is not None else torch.cuda.current_stream())
     return int(ev.cuda_event)
+
+
+def pkv_selftest_bounded_wait(status: torch.Tensor, timeout_us: int = 2000, stream=None) -> None:
+    """Run the bounded-wait self-test: a wait on an mbarrier nothing arrives
+    on gives up after ``timeout_us`` and ORs PKV_DEV_TIMEOUT into ``status``."""
+    _want(status, torch.int32, 1, "status")
+    _check(LIB.pkv_selftest_bounded_wait(_ptr(status), int(timeout_us), _stream(stream)), "pkv_selftest_bounded_wait")
 
 
 def pkv_read_status(status: torch.Tensor, stream=None) -> int:

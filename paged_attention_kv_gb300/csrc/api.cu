@@ -1,13 +1,41 @@
-// Host-only entry points of the C ABI: pool sizing, status read-back and
-// status strings.
+// Entry points of the C ABI outside the attention path: pool sizing,
+// status read-back, status strings, and the bounded-wait self-test.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "pagedkv.h"
+#include "pkv_device.cuh"
 #include "pkv_host.h"
 
 using namespace pkv;
+
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on, with the same
+// bounded wait every pipeline stage uses, so the give-up path (status bit,
+// abort flag, kernel returns) runs without a stuck pipeline.
+__global__ void selftest_wait_kernel(int32_t *status, unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    volatile int *abort = &abort_flag;
+    if (mbar_wait(&bar, 0, status, abort, timeout_ns)) raise_status(status, PKV_DEV_OVERFLOW);  // cannot complete
+    mbar_arrive(&bar);  // complete the phase before the CTA exits
+}
+
+}  // namespace
+
+extern "C" PKV_API int pkv_selftest_bounded_wait(int32_t *status, uint32_t timeout_us, void *stream) {
+    if (!status) return PKV_E_NULL;
+    if (!aligned(status, 4)) return PKV_E_ALIGN;
+    if (timeout_us == 0 || timeout_us > 1000000) return PKV_E_DIMS;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, 1000ull * timeout_us);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
 
 // Page 2 ("LLM Engine 构造函数", KV-cache-manager note) gives the bytes of one
 // block of one layer as 2 * block_size * num_kv_heads * head_size *

@@ -60,10 +60,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase of `parity` to complete. Gives up (false) when
-// *abort becomes nonzero, or after kWaitTimeoutNs, in which case it raises
+// *abort becomes nonzero, or after timeout_ns (kWaitTimeoutNs unless a
+// self-test passes a shorter limit), in which case it raises
 // PKV_DEV_TIMEOUT and sets *abort so the rest of the CTA stops waiting too.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status,
-                                          volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status, volatile int *abort,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
@@ -71,7 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             raise_status(status, PKV_DEV_TIMEOUT);
             *abort = 1;
             return false;

@@ -344,3 +344,48 @@ def test_chunk_pairs_with_and_without_a_second_tile(shape):
     seq = [t, 3 * t + 700, 5 * t + 45, 2 * t + 128, 900]
     batch = _custom(shape, seq, ql, 600 + g)
     _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+def test_a_wait_that_never_completes_is_reported_and_the_context_survives():
+    """Failure detection without a fault: the self-test's wait on a barrier
+    that nothing arrives on gives up after 2 ms, the status word carries
+    PKV_DEV_TIMEOUT, and the next attention step runs normally."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    pkv.pkv_selftest_bounded_wait(status, timeout_us=2000)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 1.0
+    assert pkv.pkv_read_status(status) == pkv.PKV_DEV_TIMEOUT
+    batch = _custom(LLAMA, [300, 40], [1, 2], 610)
+    _check_full(batch, device_tensors(batch, generate_on="cpu"))
+
+
+def test_duplicate_slots_stay_inside_their_slot():
+    """Two tokens mapped to one slot (an invalid slot mapping that the write
+    does not detect): every 16-byte chunk of that slot ends up as one of the
+    two tokens' chunks, and no other byte of the pool changes."""
+    batch = _custom(TINY, [40, 70], [1, 1], 620)
+    ten = device_tensors(batch, generate_on="cpu")
+    pool = ten["kv_cache"].clone()
+    before = wl.bf16_bits(pool).copy()
+    k = torch.randn(3, TINY.num_kv_heads, TINY.head_size).to(torch.bfloat16).cuda()
+    v = torch.randn(3, TINY.num_kv_heads, TINY.head_size).to(torch.bfloat16).cuda()
+    slot = 5 * 16 + 7
+    slots = torch.tensor([slot, slot, 9 * 16 + 1], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write(k, v, slots, pool, status)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(status) == 0
+    after = wl.bf16_bits(pool)
+    kb, vb = wl.bf16_bits(k), wl.bf16_bits(v)
+    changed = np.argwhere(before != after)
+    blocks_rows = {(int(c[0]), int(c[3])) for c in changed}
+    assert blocks_rows <= {(5, 7), (9, 1)}
+    for kv, src in ((0, kb), (1, vb)):
+        got = after[5, kv, :, 7, :].reshape(TINY.num_kv_heads, -1, 8)  # 16-byte chunks
+        a0 = src[0].reshape(TINY.num_kv_heads, -1, 8)
+        a1 = src[1].reshape(TINY.num_kv_heads, -1, 8)
+        ok = np.all(got == a0, axis=2) | np.all(got == a1, axis=2)
+        assert ok.all()
+        assert np.array_equal(after[9, kv, :, 1, :], src[2])
