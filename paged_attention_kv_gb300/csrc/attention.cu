@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
                 ok = true;
                 const long long rows = (long long)n * g;
                 if (a.chunk_ok && rows >= kChunkRows) {
-                    tiles = (unsigned long long)((rows + kChunkPairRows - 1) / kChunkPairRows) << 32;
+                    tiles = (unsigned long long)((rows + kChunkRows - 1) / kChunkRows) << 32;
                     atomicMax(&s_kvmax, L);
                     s_cas_ok = 0;  // the shared-prefix pass covers split-KV rows only
                 } else {
@@ -322,9 +322,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0 && P0 > 0)  // the prefix tiles
         work += ((long long)a.num_tokens * g + kRowsPerTile - 1) / kRowsPerTile * Hkv * P0;
     const int kvmax = s_kvmax;
-    auto chunk_kv_end = [&](int r, int pair) {  // keys seen by the pair's last row
-        const long long last_row =
-            min((long long)req_n[r] * g - 1, (long long)pair * kChunkPairRows + kChunkPairRows - 1);
+    auto chunk_kv_end = [&](int r, int mt) {  // keys seen by the tile's last row
+        const long long last_row = min((long long)req_n[r] * g - 1, (long long)mt * kChunkRows + kChunkRows - 1);
         return req_L[r] - req_n[r] + (int)(last_row / g) + 1;
     };
     auto chunk_bucket = [&](int kv_end) {  // longest first
@@ -506,7 +505,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         if (gi >= n_cgroups) continue;
         const int n = req_n[r];
         const long long rows = (long long)n * g;
-        const int nv = (int)min((long long)kChunkPairRows, rows - (long long)mt * kChunkPairRows);
+        const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
         for (int h = 0; h < Hkv; ++h) {
             const int idx = first + h;
             ChunkItem c;
@@ -689,12 +688,8 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
             if (lane == 0) {
                 uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
                 mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-#pragma unroll
-                for (int bx = 0; bx < S::kBoxes; ++bx) {
-                    tma_load_3d(st + bx * 2048, kv_map, bx * 64, h * PKV_BLOCK_SIZE, blk, &full[stage]);
-                    tma_load_3d(st + S::kTileBytes + bx * 2048, kv_map, bx * 64,
-                                (Hkv + h) * PKV_BLOCK_SIZE, blk, &full[stage]);
-                }
+                tma_load_4d(st, kv_map, 0, h * PKV_BLOCK_SIZE, 0, blk, &full[stage]);
+                tma_load_4d(st + S::kTileBytes, kv_map, 0, (Hkv + h) * PKV_BLOCK_SIZE, 0, blk, &full[stage]);
             }
             __syncwarp();
             ++e;
@@ -1126,13 +1121,19 @@ long long default_part_rows_cap(int sm_count, long long num_tokens, int num_q_he
     return max(grid_rows, prefix_rows);
 }
 
+// The pool [NB][2][Hkv][16][D] as a 4-D map {64 columns, row of the block
+// (kv * Hkv + head) * 16 + token, 64-column half, block}; one box is a whole
+// (block, K or V, head): 16 rows x D columns, landing in shared memory as
+// D / 64 consecutive 2 KiB pieces [half][16 rows][128 B] (128-byte swizzle).
+// One copy per block and head instead of one per 64 columns: the copy engine
+// spends a fixed cost per box.
 int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &d) {
     const cuuint64_t rows_per_block = 2ull * d.num_kv_heads * PKV_BLOCK_SIZE;
-    cuuint64_t dims[3] = {(cuuint64_t)d.head_size, rows_per_block, (cuuint64_t)d.num_blocks};
-    cuuint64_t strides[2] = {(cuuint64_t)d.head_size * 2, rows_per_block * d.head_size * 2};
-    cuuint32_t box[3] = {64, PKV_BLOCK_SIZE, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv_cache), dims, strides,
+    cuuint64_t dims[4] = {64, rows_per_block, (cuuint64_t)d.head_size / 64, (cuuint64_t)d.num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)d.head_size * 2, 128, rows_per_block * d.head_size * 2};
+    cuuint32_t box[4] = {64, PKV_BLOCK_SIZE, (cuuint32_t)d.head_size / 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv_cache), dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;

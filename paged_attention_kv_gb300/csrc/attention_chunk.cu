@@ -2,28 +2,38 @@
 // new tokens in one step (chunked prefill, "Inside vLLM", page 1, "Chunked
 // prefill"; V1 mixes such chunks with decode tokens, "Scheduler").
 //
-// A work item is a pair of 128-row query tiles A and B (rows = tokens x the
-// q heads of one GQA group, token-major; B is the next 128 rows of the same
-// request and may be empty) of one request and kv head. Both tiles run over
-// one stream of 128-key K/V tiles (B, later in the chunk, sees as many keys
-// as A or more), and take turns on the tensor core:
-//   S_t = Q_t K^T   tcgen05.mma (M=128, N=128, K=16 steps), bf16 operands in
-//                   128B-swizzled shared memory, fp32 accumulator in TMEM;
-//   softmax         four warps per tile, one thread per row (its TMEM lane):
-//                   causal mask, exp2 against a running reference max that
-//                   only moves (and rescales O_t) when a row max grows by
-//                   more than 2^8; P_t goes back into the TMEM columns of S_t
-//                   as bf16 pairs;
-//   O_t += P_t V    tcgen05.mma (M=128, N=D) with A = P_t read from TMEM and
-//                   B = V MN-major straight from its TMA tile; O_t stays in
-//                   TMEM.
-// The MMA warp issues S_A(0), S_B(0), then PV_A(j), S_A(j+1), PV_B(j),
-// S_B(j+1), ...: while the softmax warps of one tile work, the tensor core
-// can run the other tile's products. Warps: 0 TMA producer (Q tiles; K and V tiles of 8 blocks, one
-// box per 64 columns of each block), 1 MMA issuer (one elected lane) and
-// TMEM owner, 2-5 softmax and output of tile A, 6-9 of tile B. Every wait is
-// bounded; on a timeout the CTA raises PKV_DEV_TIMEOUT, stops, lets its
-// in-flight copies and MMAs finish and frees its TMEM.
+// A work item is one 128-row query tile (rows = tokens x the q heads of one
+// GQA group, token-major) of one request and kv head, over all keys its rows
+// may see, in 128-key tiles. Per key tile x:
+//   S(x) = Q K(x)^T   tcgen05.mma (M=128, N=128, K=16 steps), bf16 operands
+//                     in 128B-swizzled shared memory, fp32 accumulator in
+//                     TMEM; two S buffers, so S(x+1) is ready while the
+//                     softmax works on S(x);
+//   softmax           sixteen warps, four per TMEM lane quadrant: a row is
+//                     one lane, its 128 keys split into four 32-key parts,
+//                     one per warp; the four partial row maxima meet in
+//                     shared memory. Causal mask, exp2 against a running
+//                     reference max that only moves (and rescales O) when a
+//                     row max grows by more than 2^8; P(x) goes to one of two
+//                     P buffers in TMEM as bf16 pairs;
+//   O += P(x) V(x)    tcgen05.mma (M=128, N=D) with A = P(x) read from TMEM
+//                     and B = V MN-major straight from its TMA tile; O stays
+//                     in TMEM.
+// K and V tiles arrive one copy per block (16 keys x D), as D / 64 pieces of
+// [16 keys][64 columns]; the S product runs as two N=64 halves, tokens 0-7
+// of the eight blocks and tokens 8-15, so S, P and the PV product's K steps
+// see the tile's keys in the order (token half, block, token): column c <
+// 64 is key 16 * (c / 8) + c % 8, column c >= 64 key 16 * ((c - 64) / 8) +
+// 8 + c % 8. Masks follow the same order.
+// The softmax of tile x waits only for S(x) and for the P buffer of tile x-2
+// to be consumed; the tensor core runs PV(x-1) and S(x+1) meanwhile. One
+// warp per row would leave each SM sub-partition a single long dependency
+// chain per tile; four shorter ones interleave. Warps: 0-15 softmax and
+// output (warp w: lane quadrant w % 4, key part w / 4), 16 TMA producer (Q
+// tile; K and V tiles of 8 blocks, one box per 64 columns of each block; K
+// runs a tile ahead of V), 17 MMA issuer (one elected lane) and TMEM owner. Every wait is bounded; on a
+// timeout the CTA raises PKV_DEV_TIMEOUT, stops, lets its in-flight copies
+// and MMAs finish and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -38,54 +48,59 @@
 namespace pkv {
 namespace {
 
-// Warps 0-3 softmax of tile A, 4-7 of tile B (one warpgroup each), 8 TMA
-// producer, 9 MMA issuer, 10-11 idle (they only give their registers to
-// the softmax warpgroups).
-constexpr int kChunkThreads = 384;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-// Register budget per thread after the split (launch allocation: 168 per
-// thread at 384 threads). 256 softmax threads x 192 + 128 x 120 = 64512 =
-// 384 x 168: the decreases return exactly what the increases take; per
-// sub-partition 192 + 192 + 120 = 504 <= 512.
-constexpr uint32_t kRegsSoftmax = 192, kRegsOther = 120;
-constexpr uint32_t kTmemCols = 512;       // S_A | S_B | O_A | O_B
-constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8
-constexpr int kSoftmaxArrivals = 4;       // warps per tile
 
-// mbarrier slots. Per tile t (0 = A, 1 = B): S ready, P stored, the item's
-// last PV done, O read out. K and V have rings of kStages slots each; a K
-// slot is released once the last S product reading it is done, a V slot
-// after the last PV, so K runs a tile ahead of V.
-template <int kStages>
+constexpr int kParts = 4;                          // softmax warps per TMEM lane quadrant
+constexpr int kSoftmaxWarps = 4 * kParts;
+constexpr int kPartKeys = kChunkKeys / kParts;     // keys of one warp's part
+static_assert(kParts == 4 && kChunkKeys == 128, "the key order assumes four 32-key parts of a 128-key tile");
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kChunkThreads = 32 * (kSoftmaxWarps + 2);
+// TMEM columns: S0 | S1 (fp32, 128 each) | P0 | P1 (bf16 pairs, 64 each) | O (D).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColP = 256, kColO = 384;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8
+
+// mbarrier slots. S, P and PV-done by buffer (tile parity); a K ring of
+// kK slots and a V ring of kV; a K slot is released once its S product is
+// done, a V slot after its PV product. XBar: per lane quadrant and exchange
+// parity, the four part warps' partial values are in shared memory.
+template <int kK, int kV>
 struct ChunkBars {
     static constexpr int kQFull = 0, kQTaken = 1, kQEmpty = 2;
     static constexpr int kKFull = 3;
-    static constexpr int kVFull = kKFull + kStages;
-    static constexpr int kKEmpty = kVFull + kStages;
-    static constexpr int kVEmpty = kKEmpty + kStages;
-    static constexpr int kSFull = kVEmpty + kStages;  // [2]
-    static constexpr int kPFull = kSFull + 2;          // [2]
-    static constexpr int kODone = kPFull + 2;          // [2]
-    static constexpr int kOFree = kODone + 2;          // [2]
-    static constexpr int kDrain = kOFree + 2;
-    static constexpr int kCount = kDrain + 1;
+    static constexpr int kKEmpty = kKFull + kK;
+    static constexpr int kVFull = kKEmpty + kK;
+    static constexpr int kVEmpty = kVFull + kV;
+    static constexpr int kSFull = kVEmpty + kV;  // [2]
+    static constexpr int kPFull = kSFull + 2;     // [2]
+    static constexpr int kPvDone = kPFull + 2;    // [2]
+    static constexpr int kODone = kPvDone + 2;
+    static constexpr int kOFree = kODone + 1;
+    static constexpr int kDrain = kOFree + 1;
+    static constexpr int kXBar = kDrain + 1;      // [4 quadrants][2 parities]
+    static constexpr int kCount = kXBar + 8;
 };
 
 // Item as the producer hands it to the other roles.
 struct ChunkDesc {
-    int item, r, pair, h, q0, n, L, nv_a, nv_b, kv_end_a, kv_end_b, nt_a, nt_b, pad[3];
+    int item, r, mt, h, q0, n, L, nv, kv_end, nt, pad[6];
 };
 
 template <int D>
 struct ChunkSmem {
-    static constexpr int kStages = D == 128 ? 2 : 4;
-    using Bars = ChunkBars<kStages>;
-    static constexpr int kHalf = 16384;             // 128 rows x 128 B (64 bf16 columns)
+    // K ring three deep at D = 128 (the S products wait on K more than the
+    // PV products wait on V); that is what fits next to Q and the V ring.
+    static constexpr int kKStages = D == 128 ? 3 : 4;
+    static constexpr int kVStages = D == 128 ? 2 : 4;
+    using Bars = ChunkBars<kKStages, kVStages>;
+    static constexpr int kHalf = 16384;             // Q: 128 rows x 128 B (64 bf16 columns)
     static constexpr int kTile = (D / 64) * kHalf;  // 128 rows x D bf16
-    static constexpr int kOffQ = 0;                 // Q_A, Q_B
-    static constexpr int kOffK = kOffQ + 2 * kTile;
-    static constexpr int kOffV = kOffK + kStages * kTile;
-    static constexpr int kOffDesc = kOffV + kStages * kTile;
+    static constexpr int kBlk = (D / 64) * 2048;    // K / V: one block [D / 64][16 keys][128 B]
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kTile;
+    static constexpr int kOffV = kOffK + kKStages * kTile;
+    static constexpr int kOffX = kOffV + kVStages * kTile;  // float [2][kParts][128]: partial maxima / sums
+    static constexpr int kOffDesc = kOffX + 2 * kParts * kChunkRows * 4;
     static constexpr int kOffBar = kOffDesc + (int)sizeof(ChunkDesc);
     static constexpr int kOffTmem = kOffBar + Bars::kCount * 8;
     static constexpr int kBytes = kOffTmem + 16;
@@ -93,12 +108,6 @@ struct ChunkSmem {
 };
 static_assert(ChunkSmem<128>::kAlloc <= 232448, "chunk kernel shared memory");
 static_assert(ChunkSmem<64>::kAlloc <= 232448, "chunk kernel shared memory");
-
-// Keys visible to the last valid row of a tile that starts at row `row0` of
-// a request (n new tokens, context L, GQA group g) and holds nv rows.
-__device__ __forceinline__ int chunk_tile_kv_end(int n, int L, int g, int row0, int nv) {
-    return L - n + (row0 + nv - 1) / g + 1;
-}
 
 // A bounded wait that the whole warp leaves with one answer (the warp runs
 // warp-collective TMEM instructions afterwards).
@@ -112,7 +121,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
              const ChunkArgs a) {
     using S = ChunkSmem<D>;
     using B = typename S::Bars;
-    constexpr int kStages = S::kStages;
+    constexpr int kKStages = S::kKStages, kVStages = S::kVStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -120,8 +129,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     uint64_t *q_full = bar + B::kQFull, *q_taken = bar + B::kQTaken, *q_empty = bar + B::kQEmpty;
     uint64_t *k_full = bar + B::kKFull, *v_full = bar + B::kVFull;
     uint64_t *k_empty = bar + B::kKEmpty, *v_empty = bar + B::kVEmpty;
-    uint64_t *s_full = bar + B::kSFull, *p_full = bar + B::kPFull;
+    uint64_t *s_full = bar + B::kSFull, *p_full = bar + B::kPFull, *pv_done = bar + B::kPvDone;
     uint64_t *o_done = bar + B::kODone, *o_free = bar + B::kOFree, *drain = bar + B::kDrain;
+    uint64_t *xbar = bar + B::kXBar;
+    float *xbuf = reinterpret_cast<float *>(smem + S::kOffX);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffTmem);
     ChunkDesc *desc = reinterpret_cast<ChunkDesc *>(smem + S::kOffDesc);
     volatile int *abort = &s_abort;
@@ -133,21 +144,25 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     if (threadIdx.x == 0) {
         s_abort = 0;
         mbar_init(q_full, 1);
-        mbar_init(q_taken, 1 + 2 * kSoftmaxArrivals);  // the MMA thread and eight softmax warps
+        mbar_init(q_taken, 1 + kSoftmaxWarps);  // the MMA warp and the softmax warps
         mbar_init(q_empty, 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], kSoftmaxArrivals);
-            mbar_init(&o_done[t], 1);
-            mbar_init(&o_free[t], kSoftmaxArrivals);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], kSoftmaxWarps);
+            mbar_init(&pv_done[b], 1);
         }
+        mbar_init(o_done, 1);
+        mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], kParts);
         mbar_fence_init();
     }
     // The barrier setup above overlaps the previous kernel; the work list it
@@ -163,350 +178,346 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     tmem_fence_after_sync();
     const uint32_t tm = *tmem_slot;
 
-    if (warp >= 2 * kSoftmaxArrivals) {
-        setmaxnreg_dec<kRegsOther>();
-        if (warp == kProducerWarp) {
-            // ------------------------------ producer ------------------------------
-            if (lane == 0) {
-                tma_prefetch_desc(&kv_map);
-                tma_prefetch_desc(&q_map);
+    if (warp == kProducerWarp) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&kv_map);
+            tma_prefetch_desc(&q_map);
+        }
+        const int Hkv = a.num_kv_heads;
+        constexpr int kTileBlocks = kChunkKeys / PKV_BLOCK_SIZE;  // 8 blocks per key tile
+        uint32_t jt = 0;  // K/V tiles of the items so far
+        uint32_t k_issued = 0, v_issued = 0;
+        bool ok = true;
+        // Global reads that a load depends on are issued ahead of it: the
+        // next item is claimed while the current one issues its last K tile,
+        // and each key tile's block ids are read three tiles ahead (lane b <
+        // 8 holds block b of the tile), so no copy waits on a round trip to
+        // memory once the slot is free.
+        int it_raw = 0;
+        if (lane == 0) it_raw = atomicAdd(&a.header->next_chunk_item, 1);
+        int it = __shfl_sync(0xffffffffu, it_raw, 0);
+        ChunkItem w{};
+        if (it < n_items) w = a.items[it];
+        for (int k = 0; ok; ++k) {
+            const int r = w.a.x, mt = w.a.y, h = w.a.z, kv_end = w.a.w;
+            const int q0 = w.b.x, n = w.b.y, L = w.b.z, nv = w.b.w;
+            const int nt = it < n_items ? (kv_end + kChunkKeys - 1) / kChunkKeys : 0;
+            const int kvb = (kv_end + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+            const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
+            // Block id of lane `lane` in key tile t; past the request's
+            // blocks it is a.num_blocks, past the map: TMA fills zeros.
+            auto fetch = [&](int t) {
+                const int kb = t * kTileBlocks + lane;
+                return (lane < kTileBlocks && t < nt && kb < kvb) ? __ldg(bt + kb) : a.num_blocks;
+            };
+            int id0 = fetch(0), id1 = fetch(1), id2 = fetch(2);
+            if (!mbar_wait(q_taken, (k & 1) ^ 1, status, abort) || !mbar_wait(q_empty, (k & 1) ^ 1, status, abort)) {
+                ok = false;
+                break;
             }
-            const int Hkv = a.num_kv_heads;
-            uint32_t jt = 0;                   // K/V tiles of the items so far
-            uint32_t k_issued = 0, v_issued = 0;
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                int it = 0;
-                if (lane == 0) it = atomicAdd(&a.header->next_chunk_item, 1);
-                it = __shfl_sync(0xffffffffu, it, 0);
-                if (!mbar_wait(q_taken, (k & 1) ^ 1, status, abort) || !mbar_wait(q_empty, (k & 1) ^ 1, status, abort)) {
+            if (it >= n_items) {
+                if (lane == 0) {
+                    desc->item = -1;
+                    mbar_arrive(q_full);
+                }
+                break;
+            }
+            if (lane == 0) {
+                ChunkDesc d;
+                d.item = it; d.r = r; d.mt = mt; d.h = h; d.q0 = q0; d.n = n; d.L = L; d.nv = nv;
+                d.kv_end = kv_end; d.nt = nt;
+                *desc = d;
+                mbar_arrive_expect_tx(q_full, kChunkRows * D * 2);
+#pragma unroll
+                for (int bx = 0; bx < D / 64; ++bx)
+                    tma_load_3d(smem + S::kOffQ + bx * S::kHalf, &q_map, bx * 64, h * g, q0 + mt * (kChunkRows / g),
+                                q_full);
+            }
+            __syncwarp();
+            // K or V of key tile j into its ring slot: eight blocks, one box
+            // each.
+            auto load = [&](bool is_v, int j, int blk) {
+                const uint32_t x = jt + j;
+                const int stages = is_v ? kVStages : kKStages;
+                const int st = x % stages;
+                uint64_t *full = is_v ? &v_full[st] : &k_full[st];
+                if (!mbar_wait(is_v ? &v_empty[st] : &k_empty[st], ((x / stages) & 1) ^ 1, status, abort))
+                    return false;
+                if (blk < 0 || blk > a.num_blocks || (blk == a.num_blocks && j * kTileBlocks + lane < kvb)) {
+                    if (lane < kTileBlocks) raise_status(status, PKV_DEV_BAD_BLOCK);
+                    blk = a.num_blocks;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(full, kChunkKeys * D * 2);
+                __syncwarp();
+                if (lane < kTileBlocks) {
+                    uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * S::kBlk;
+                    tma_load_4d(dst, &kv_map, 0, (is_v ? Hkv + h : h) * PKV_BLOCK_SIZE, 0, blk, full);
+                }
+                __syncwarp();
+                if (is_v) ++v_issued; else ++k_issued;
+                return true;
+            };
+            auto claim_next = [&]() {
+                if (lane == 0) it_raw = atomicAdd(&a.header->next_chunk_item, 1);
+            };
+            // K runs one tile ahead of V; V of tile j reuses K's block ids.
+            ok = load(false, 0, id0);
+            if (nt == 1) claim_next();
+            for (int j = 0; j < nt && ok; ++j) {
+                if (j + 1 < nt) {
+                    ok = load(false, j + 1, id1);
+                    if (j + 2 == nt) claim_next();
+                }
+                if (ok) ok = load(true, j, id0);
+                id0 = id1;
+                id1 = id2;
+                id2 = fetch(j + 3);
+            }
+            jt += nt;
+            it = __shfl_sync(0xffffffffu, it_raw, 0);
+            if (it < n_items) w = a.items[it];
+        }
+        if (!ok && lane == 0) {
+            // let copies already issued land before the CTA can leave
+            for (uint32_t x = k_issued > (uint32_t)kKStages ? k_issued - kKStages : 0; x < k_issued; ++x)
+                mbar_drain(&k_full[x % kKStages], (x / kKStages) & 1, status, diag, 0x2);
+            for (uint32_t x = v_issued > (uint32_t)kVStages ? v_issued - kVStages : 0; x < v_issued; ++x)
+                mbar_drain(&v_full[x % kVStages], (x / kVStages) & 1, status, diag, 0x2);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------ MMA issuer -----------------------------
+        // The whole warp walks the schedule with the same values (so
+        // descriptors and TMEM addresses stay warp-uniform); one elected lane
+        // issues every tcgen05.mma and commit.
+        constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys / 2, 0, 0);
+        constexpr uint32_t kIdPV = umma_idesc_bf16(128, D, 0, 1);
+        const uint32_t q_s = smem_u32(smem + S::kOffQ);
+        const uint32_t k_s = smem_u32(smem + S::kOffK), v_s = smem_u32(smem + S::kOffV);
+        uint32_t jt = 0;  // key tiles of the items so far (global tile index base)
+        uint32_t n_items_done = 0;
+        bool ok = true;
+        // S(x) = Q K(x)^T into S buffer x & 1, as two N=64 products: tokens
+        // 0-7 of the eight blocks (8-row groups one block apart), then tokens
+        // 8-15. Its K slot is released when the product is done (it is the
+        // slot's only reader).
+        auto issue_s = [&](uint32_t x) {
+            const int st = x % kKStages;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t qd = umma_desc_sw128(q_s + (kk / 4) * S::kHalf + (kk % 4) * 32, 16, 1024);
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    umma_bf16_warp(tm + (x & 1) * kChunkKeys + hr * (kChunkKeys / 2), qd,
+                                   umma_desc_sw128(k_s + st * S::kTile + (kk / 4) * 2048 + (kk % 4) * 32 + hr * 1024,
+                                                   16, S::kBlk),
+                                   kIdS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit_warp(&s_full[x & 1]);
+            umma_commit_warp(&k_empty[st]);
+        };
+        for (int k = 0; ok; ++k) {
+            if (!warp_wait(q_full, k & 1, status, abort)) { ok = false; break; }
+            const ChunkDesc d = *desc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_taken);
+            if (d.item < 0) break;
+            const int nt = d.nt;
+            // S of the first two key tiles
+            for (int j = 0; j < min(nt, 2) && ok; ++j) {
+                const uint32_t x = jt + j;
+                if (!warp_wait(&k_full[x % kKStages], (x / kKStages) & 1, status, abort)) { ok = false; break; }
+                tmem_fence_after_sync();
+                issue_s(x);
+            }
+            if (!ok) break;
+            if (nt <= 2) umma_commit_warp(q_empty);  // every S of the item is issued
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t x = jt + j;
+                const int st = x % kVStages;
+                if (!warp_wait(&p_full[x & 1], (x >> 1) & 1, status, abort)) { ok = false; break; }
+                if (j == 0 && n_items_done > 0 && !warp_wait(o_free, (n_items_done - 1) & 1, status, abort)) {
                     ok = false;
                     break;
                 }
-                if (it >= n_items) {
-                    if (lane == 0) {
-                        desc->item = -1;
-                        mbar_arrive(q_full);
-                    }
-                    break;
+                if (!warp_wait(&v_full[st], (x / kVStages) & 1, status, abort)) { ok = false; break; }
+                tmem_fence_after_sync();
+                // O += P(x) V(x): P from TMEM (64 columns of bf16 pairs), V
+                // MN-major; K step kk takes tokens 0-7 (kk < 4) or 8-15 of
+                // blocks 2 (kk % 4) and 2 (kk % 4) + 1, as S ordered them.
+#pragma unroll
+                for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
+                    const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + (kk % 4) * 2 * S::kBlk + (kk / 4) * 1024,
+                                                        2048, S::kBlk);
+                    umma_bf16_tmem_a_warp(tm + kColO, tm + kColP + (x & 1) * 64 + kk * 8, bd, kIdPV,
+                                          (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                const ChunkItem w = a.items[it];
-                const int r = w.a.x, pair = w.a.y, h = w.a.z;
-                const int q0 = w.b.x, n = w.b.y, L = w.b.z, nv = w.b.w;  // nv: valid rows of the pair
-                const int nv_a = min(kChunkRows, nv), nv_b = nv - nv_a;
-                const int row0 = pair * kChunkPairRows;
-                const int kv_end_a = chunk_tile_kv_end(n, L, g, row0, nv_a);
-                const int kv_end_b = nv_b > 0 ? chunk_tile_kv_end(n, L, g, row0 + kChunkRows, nv_b) : 0;
-                const int nt_a = (kv_end_a + kChunkKeys - 1) / kChunkKeys;
-                const int nt_b = (kv_end_b + kChunkKeys - 1) / kChunkKeys;
-                const int nt = max(nt_a, nt_b);
-                const int kvb = (max(kv_end_a, kv_end_b) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-                if (lane == 0) {
-                    ChunkDesc d;
-                    d.item = it; d.r = r; d.pair = pair; d.h = h; d.q0 = q0; d.n = n; d.L = L;
-                    d.nv_a = nv_a; d.nv_b = nv_b; d.kv_end_a = kv_end_a; d.kv_end_b = kv_end_b;
-                    d.nt_a = nt_a; d.nt_b = nt_b;
-                    *desc = d;
-                    const int tiles = nv_b > 0 ? 2 : 1;
-                    mbar_arrive_expect_tx(q_full, (uint32_t)tiles * kChunkRows * D * 2);
-                    for (int t = 0; t < tiles; ++t) {
-                        const int tok = q0 + (row0 + t * kChunkRows) / g;
-    #pragma unroll
-                        for (int bx = 0; bx < D / 64; ++bx)
-                            tma_load_3d(smem + S::kOffQ + t * S::kTile + bx * S::kHalf, &q_map, bx * 64, h * g, tok,
-                                        q_full);
-                    }
-                }
-                __syncwarp();
-                const int32_t *bt = a.block_table + (long long)r * a.max_blocks_per_req;
-                // K or V of key tile j into its ring slot: eight blocks, one box
-                // per 64 columns of each.
-                auto load = [&](bool is_v, int j) {
-                    const uint32_t x = jt + j;
-                    const int st = x % kStages;
-                    uint64_t *full = is_v ? &v_full[st] : &k_full[st];
-                    if (!mbar_wait(is_v ? &v_empty[st] : &k_empty[st], ((x / kStages) & 1) ^ 1, status, abort))
-                        return false;
-                    int blk = a.num_blocks;  // past the map: TMA fills zeros
-                    const int kb = j * (kChunkKeys / PKV_BLOCK_SIZE) + lane;
-                    if (lane < kChunkKeys / PKV_BLOCK_SIZE && kb < kvb) {
-                        blk = __ldg(bt + kb);
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            raise_status(status, PKV_DEV_BAD_BLOCK);
-                            blk = a.num_blocks;
-                        }
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(full, kChunkKeys * D * 2);
-                    __syncwarp();
-                    if (lane < kChunkKeys / PKV_BLOCK_SIZE) {
-                        uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * 2048;
-                        const int row = (is_v ? Hkv + h : h) * PKV_BLOCK_SIZE;
-    #pragma unroll
-                        for (int bx = 0; bx < D / 64; ++bx) tma_load_3d(dst + bx * S::kHalf, &kv_map, bx * 64, row, blk, full);
-                    }
-                    __syncwarp();
-                    if (is_v) ++v_issued; else ++k_issued;
-                    return true;
-                };
-                // K runs one tile ahead of V.
-                ok = load(false, 0);
-                for (int j = 0; j < nt && ok; ++j) {
-                    if (j + 1 < nt) ok = load(false, j + 1);
-                    if (ok) ok = load(true, j);
-                }
-                jt += nt;
-            }
-            if (!ok && lane == 0) {
-                // let copies already issued land before the CTA can leave
-                for (uint32_t x = k_issued > (uint32_t)kStages ? k_issued - kStages : 0; x < k_issued; ++x)
-                    mbar_drain(&k_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
-                for (uint32_t x = v_issued > (uint32_t)kStages ? v_issued - kStages : 0; x < v_issued; ++x)
-                    mbar_drain(&v_full[x % kStages], (x / kStages) & 1, status, diag, 0x2);
-            }
-        } else if (warp == kMmaWarp) {
-            // ------------------------------ MMA issuer -----------------------------
-            // The whole warp runs this loop with the same values (so descriptors
-            // and TMEM addresses stay warp-uniform); one elected lane issues
-            // every tcgen05.mma and commit.
-            {
-                constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys, 0, 0);
-                constexpr uint32_t kIdPV = umma_idesc_bf16(128, D, 0, 1);
-                const uint32_t q_s = smem_u32(smem + S::kOffQ);
-                const uint32_t k_s = smem_u32(smem + S::kOffK), v_s = smem_u32(smem + S::kOffV);
-                uint32_t jt = 0;                 // K/V tiles consumed so far
-                uint32_t n_p[2] = {0, 0};        // P handoffs taken per tile
-                uint32_t n_items_t[2] = {0, 0};  // items finished per tile
-                bool ok = true;
-                // S_t(x) = Q_t K(x)^T into TMEM columns t * 128
-                auto issue_s = [&](int t, uint32_t x) {
-                    const int st = x % kStages;
-    #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * S::kHalf + (kk % 4) * 32;
-                        umma_bf16_warp(tm + t * kChunkKeys, umma_desc_sw128(q_s + t * S::kTile + off, 16, 1024),
-                                       umma_desc_sw128(k_s + st * S::kTile + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit_warp(&s_full[t]);
-                };
-                for (int k = 0; ok; ++k) {
-                    if (!warp_wait(q_full, k & 1, status, abort)) { ok = false; break; }
-                    const ChunkDesc d = *desc;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(q_taken);
-                    if (d.item < 0) break;
-                    const int nt_t[2] = {d.nt_a, d.nt_b};
-                    const int nt = max(d.nt_a, d.nt_b);
-                    int s_left = d.nt_a + d.nt_b;  // S products of this item still to issue
-                    // S of the first key tile, for both tiles
-                    if (!warp_wait(&k_full[jt % kStages], (jt / kStages) & 1, status, abort)) { ok = false; break; }
+                umma_commit_warp(&pv_done[x & 1]);
+                umma_commit_warp(&v_empty[st]);
+                if (j == nt - 1) umma_commit_warp(o_done);
+                if (j + 2 < nt) {
+                    // S(x+2) reuses the S buffer of x, which the softmax read
+                    // before it stored P(x).
+                    const uint32_t y = x + 2;
+                    if (!warp_wait(&k_full[y % kKStages], (y / kKStages) & 1, status, abort)) { ok = false; break; }
                     tmem_fence_after_sync();
-    #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (nt_t[t] > 0) {
-                            issue_s(t, jt);
-                            if (--s_left == 0) umma_commit_warp(q_empty);
-                        }
-                    }
-                    umma_commit_warp(&k_empty[jt % kStages]);  // both S products of key tile 0 are issued
-                    for (int j = 0; j < nt && ok; ++j) {
-                        const uint32_t x = jt + j;
-                        const int st = x % kStages;
-                        bool v_ready = false, k_next_ready = false;
-    #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            if (j >= nt_t[t]) continue;
-                            if (!warp_wait(&p_full[t], n_p[t] & 1, status, abort)) { ok = false; break; }
-                            ++n_p[t];
-                            if (j == 0 && n_items_t[t] > 0 &&
-                                !warp_wait(&o_free[t], (n_items_t[t] - 1) & 1, status, abort)) {
-                                ok = false;
-                                break;
-                            }
-                            if (!v_ready) {
-                                if (!warp_wait(&v_full[st], (x / kStages) & 1, status, abort)) { ok = false; break; }
-                                v_ready = true;
-                            }
-                            tmem_fence_after_sync();
-                            // O_t += P_t V: P_t from TMEM (64 columns of bf16 pairs), V MN-major.
-    #pragma unroll
-                            for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
-                                const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + kk * 2048, S::kHalf, 1024);
-                                umma_bf16_tmem_a_warp(tm + 256 + t * D, tm + t * kChunkKeys + kk * 8, bd, kIdPV,
-                                                      (j > 0 || kk > 0) ? 1u : 0u);
-                            }
-                            if (j == nt_t[t] - 1) {
-                                umma_commit_warp(&o_done[t]);
-                                ++n_items_t[t];
-                            }
-                            if (t == 1 || nt_t[1] <= j) umma_commit_warp(&v_empty[st]);  // last PV on this V tile
-                            if (j + 1 < nt_t[t]) {
-                                // S_t(j+1) follows PV_t(j), which read P_t from the same columns
-                                if (!k_next_ready) {
-                                    const uint32_t y = x + 1;
-                                    if (!warp_wait(&k_full[y % kStages], (y / kStages) & 1, status, abort)) {
-                                        ok = false;
-                                        break;
-                                    }
-                                    k_next_ready = true;
-                                }
-                                issue_s(t, x + 1);
-                                if (--s_left == 0) umma_commit_warp(q_empty);
-                                if (t == 1 || nt_t[1] <= j + 1) umma_commit_warp(&k_empty[(x + 1) % kStages]);
-                            }
-                        }
-                    }
-                    jt += nt;
+                    issue_s(y);
+                    if (j + 3 == nt) umma_commit_warp(q_empty);  // that was the item's last S
                 }
-                // make sure no MMA is still writing TMEM before it is freed
-                umma_commit_warp(drain);
-                if (lane == 0) mbar_drain(drain, 0, status, diag, 0x4);
             }
-            __syncwarp();
+            jt += nt;
+            ++n_items_done;
         }
+        // make sure no MMA is still writing TMEM before it is freed
+        umma_commit_warp(drain);
+        if (lane == 0) mbar_drain(drain, 0, status, diag, 0x4);
+        __syncwarp();
     } else {
-        setmaxnreg_inc<kRegsSoftmax>();
         // --------------------------- softmax and output ---------------------------
-        const int t = warp >> 2;         // 0: tile A (warps 0-3), 1: tile B (warps 4-7)
-        const int q4 = warp & 3;        // TMEM lane quadrant this warp may access
-        const int row = q4 * 32 + lane; // query row of the tile = TMEM lane
+        constexpr int kOCols = D / kParts;  // O columns this warp rescales and writes
+        const int q4 = warp & 3;            // TMEM lane quadrant of this warp
+        const int part = warp >> 2;         // which 32 keys of each key tile
+        const int row = q4 * 32 + lane;     // query row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const uint32_t s_col = tm + lane_off + t * kChunkKeys;
-        const uint32_t o_col = tm + lane_off + 256 + t * D;
-        uint32_t n_s = 0;     // S handoffs taken
+        const uint32_t o_col = tm + lane_off + kColO + part * kOCols;
+        uint32_t jt = 0;      // key tiles of the items so far (global tile index base)
         uint32_t n_done = 0;  // items finished
-        uint32_t jt = 0;      // K/V tiles of the items seen so far
+        uint32_t n_x = 0;     // exchanges so far (the same sequence in the quadrant's four warps)
+        // The four part warps of this quadrant pool one float per row: the
+        // result is the same in all four (same values, same order).
+        auto exchange = [&](float v, bool is_max, float &res) -> bool {
+            const int par = n_x & 1;
+            float *xb = xbuf + par * (kParts * kChunkRows);
+            xb[part * kChunkRows + row] = v;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[q4 * 2 + par]);
+            if (!warp_wait(&xbar[q4 * 2 + par], (n_x >> 1) & 1, status, abort)) return false;
+            float r = xb[row];
+#pragma unroll
+            for (int p = 1; p < kParts; ++p) r = is_max ? fmaxf(r, xb[p * kChunkRows + row]) : r + xb[p * kChunkRows + row];
+            res = r;
+            ++n_x;
+            return true;
+        };
         for (int k = 0;; ++k) {
             if (!warp_wait(q_full, k & 1, status, abort)) break;
-            const int item = desc->item;
-            const int nt_a = desc->nt_a, nt_b = desc->nt_b;
-            const int nv = t ? desc->nv_b : desc->nv_a;
-            const int kv_end = t ? desc->kv_end_b : desc->kv_end_a;
-            const int kv_end_pair = max(desc->kv_end_a, desc->kv_end_b);
-            const int rho = desc->pair * kChunkPairRows + t * kChunkRows + row;
-            const int ctx0 = desc->L - desc->n;  // keys before the chunk's first token
-            const long long out_row0 = (long long)desc->q0 * a.num_q_heads + desc->h * g;
+            const ChunkDesc d = *desc;
             __syncwarp();
             if (lane == 0) mbar_arrive(q_taken);
-            if (item < 0) break;
-            const int nt_mine = t ? nt_b : nt_a;
-            const int nt = max(nt_a, nt_b);
-            // The tile whose PV comes first on the last K/V tile clears
-            // that tile's V rows past the pair's last visible key.
-            const bool zeroes = t ? (nt_a < nt) : (nt_a == nt);
-            const bool valid = row < nv;
+            if (d.item < 0) break;
+            const int nt = d.nt;
+            const int rho = d.mt * kChunkRows + row;
+            const bool valid = row < d.nv;
             const int i = valid ? rho / g : 0;
-            const int limit = valid ? ctx0 + i : kv_end - 1;
-            float m_run = -INFINITY, l = 0.f;
+            const int limit = valid ? d.L - d.n + i : d.kv_end - 1;
+            float m_run = -INFINITY, l = 0.f;  // l: this part's keys only
             bool ok = true;
-            for (int j = 0; j < nt_mine; ++j) {
-                if (!warp_wait(&s_full[t], n_s & 1, status, abort)) { ok = false; break; }
-                ++n_s;
+            for (int j = 0; j < nt; ++j) {
+                const uint32_t x = jt + j;
+                const uint32_t s_col = tm + lane_off + (x & 1) * kChunkKeys + part * kPartKeys;
+                const uint32_t p_col = tm + lane_off + kColP + (x & 1) * 64 + part * (kPartKeys / 2);
+                if (!warp_wait(&s_full[x & 1], (x >> 1) & 1, status, abort)) { ok = false; break; }
                 tmem_fence_after_sync();
-                const int key0 = j * kChunkKeys;
-                // Tiles the whole warp sees unmasked (all but the diagonal
-                // ones) take a path without per-key tests; with a positive
-                // scale the max can be taken on the raw scores.
-                const bool fast = __all_sync(0xffffffffu, key0 + kChunkKeys - 1 <= limit) && a.scale_log2 > 0.f;
-                // The row's 128 scores of this key tile: one TMEM round trip.
-                float sv[kChunkKeys / 32][32];
-#pragma unroll
-                for (int c = 0; c < kChunkKeys / 32; ++c) tmem_ld32(s_col + c * 32, sv[c]);
-#pragma unroll
-                for (int c = 0; c < kChunkKeys / 32; ++c) tmem_wait_ld_regs(sv[c]);
-                // Row max (scaled, masked), eight independent maxima.
-                float mx = -INFINITY;
+                // This part's column e holds key key0 + 16 * (e / 8) + e % 8.
+                const int key0 = j * kChunkKeys + (part & 1) * (kChunkKeys / 2) + (part >> 1) * 8;
+                // Parts the whole warp sees unmasked take a path without
+                // per-key tests; with a positive scale the max can be taken
+                // on the raw scores.
+                const bool fast = __all_sync(0xffffffffu, key0 + 55 <= limit) && a.scale_log2 > 0.f;
+                float sv[kPartKeys];
+                tmem_ld32(s_col, sv);
+                tmem_wait_ld_regs(sv);
+                // Partial row max (scaled, masked), then the row's.
+                float mx;
                 {
-                    float mxa[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mxa[e] = -INFINITY;
+                    float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     if (fast) {
 #pragma unroll
-                        for (int c = 0; c < kChunkKeys / 32; ++c)
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                mxa[(c * 16 + e) & 7] = fmax3(mxa[(c * 16 + e) & 7], sv[c][2 * e], sv[c][2 * e + 1]);
+                        for (int e = 0; e < kPartKeys / 2; ++e)
+                            mxa[e & 3] = fmax3(mxa[e & 3], sv[2 * e], sv[2 * e + 1]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < kChunkKeys / 32; ++c)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                mxa[e & 7] = fmaxf(mxa[e & 7], key0 + c * 32 + e <= limit ? sv[c][e] * a.scale_log2
-                                                                                         : -INFINITY);
+                        for (int e = 0; e < kPartKeys; ++e)
+                            mxa[e & 3] = fmaxf(mxa[e & 3], key0 + (e / 8) * 16 + e % 8 <= limit ? sv[e] * a.scale_log2
+                                                                                                : -INFINITY);
                     }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, mxa[e]);
-                    if (fast) mx *= a.scale_log2;
+                    float pm = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+                    if (fast) pm *= a.scale_log2;
+                    if (!exchange(pm, true, mx)) { ok = false; break; }
                 }
-                if (j == 0) {
-                    m_run = mx;  // key 0 is visible to every row, so this is finite
-                } else {
-                    // PV_t(j-1) completed before S_t(j) was reported, so O_t
-                    // may be rescaled in place.
-                    const bool resc = mx > m_run + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, resc)) {
-                        const float alpha = resc ? fast_exp2(m_run - mx) : 1.f;
-#pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            tmem_ld32(o_col + c * 32, o);
-                            tmem_wait_ld_regs(o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                            tmem_st32(o_col + c * 32, o);
-                        }
-                        l *= alpha;
-                        if (resc) m_run = mx;
-                    }
+                // The reference max moves only when the row max outgrows it by
+                // more than 2^8 (and on the first tile: key 0 is visible to
+                // every row, so mx is finite there).
+                const bool resc = j == 0 || mx > m_run + kRescaleThreshold;
+                const float alpha = (j > 0 && resc) ? fast_exp2(m_run - mx) : 1.f;
+                if (resc) m_run = mx;
+                const bool any_resc = j > 0 && __any_sync(0xffffffffu, resc);
+                // The P buffer of x was last read by PV(x-2).
+                if (x >= 2) {
+                    const uint32_t y = x - 2;
+                    if (!warp_wait(&pv_done[y & 1], (y >> 1) & 1, status, abort)) { ok = false; break; }
+                    tmem_fence_after_sync();
                 }
-                // P = 2^(s * scale - m_run) as bf16 pairs over the first 64
-                // columns of S_t (32 keys -> 16 columns per store).
+                // P = 2^(s * scale - m_run) as bf16 pairs (32 keys -> 16 columns).
                 {
                     const float neg_m = -m_run;
-                    float la[4] = {0.f, 0.f, 0.f, 0.f};
-                    float2 la2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    uint32_t pk[kPartKeys / 2];
+                    float sum;
+                    if (fast) {
+                        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
+                        float2 la2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                    for (int c = 0; c < kChunkKeys / 32; ++c) {
-                        uint32_t pk[16];
-                        if (fast) {
-                            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float2 x = ffma2(make_float2(sv[c][2 * e], sv[c][2 * e + 1]), sc2, nm2);
-                                const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                                la2[e & 1] = fadd2(la2[e & 1], p);
-                                pk[e] = pack_bf16x2(p.x, p.y);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int kk = key0 + c * 32 + 2 * e;
-                                const float p0 = kk <= limit ? fast_exp2(fmaf(sv[c][2 * e], a.scale_log2, neg_m)) : 0.f;
-                                const float p1 =
-                                    kk + 1 <= limit ? fast_exp2(fmaf(sv[c][2 * e + 1], a.scale_log2, neg_m)) : 0.f;
-                                la[e & 3] += p0 + p1;
-                                pk[e] = pack_bf16x2(p0, p1);
-                            }
+                        for (int e = 0; e < kPartKeys / 2; ++e) {
+                            const float2 xv = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), sc2, nm2);
+                            const float2 p = make_float2(fast_exp2(xv.x), fast_exp2(xv.y));
+                            la2[e & 1] = fadd2(la2[e & 1], p);
+                            pk[e] = pack_bf16x2(p.x, p.y);
                         }
-                        tmem_st16u(s_col + c * 16, pk);
+                        sum = (la2[0].x + la2[0].y) + (la2[1].x + la2[1].y);
+                    } else {
+                        float la[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int e = 0; e < kPartKeys / 2; ++e) {
+                            const int kk = key0 + (e / 4) * 16 + (2 * e) % 8;
+                            const float p0 = kk <= limit ? fast_exp2(fmaf(sv[2 * e], a.scale_log2, neg_m)) : 0.f;
+                            const float p1 = kk + 1 <= limit ? fast_exp2(fmaf(sv[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
+                            la[e & 3] += p0 + p1;
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        sum = (la[0] + la[1]) + (la[2] + la[3]);
                     }
-                    l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la2[0].x + la2[0].y) + (la2[1].x + la2[1].y));
+                    tmem_st16u(p_col, pk);
+                    l = fmaf(l, alpha, sum);
                 }
-                // V rows past the pair's last visible key hold other data
+                // O (this warp's columns) follows a moved reference once
+                // PV(x-1) is done, before PV(x) is issued.
+                if (any_resc) {
+                    const uint32_t y = x - 1;
+                    if (!warp_wait(&pv_done[y & 1], (y >> 1) & 1, status, abort)) { ok = false; break; }
+                    tmem_fence_after_sync();
+                    float o[kOCols];
+                    tmem_ld_cols(o_col, o);
+                    tmem_wait_ld_regs(o);
+#pragma unroll
+                    for (int e = 0; e < kOCols; ++e) o[e] *= alpha;
+                    tmem_st_cols(o_col, o);
+                }
+                // V rows past the tile's last visible key hold other data
                 // (maybe NaN); their P is 0 but 0 * NaN is not, so clear them.
-                if (zeroes && j == nt - 1) {
-                    const int first = kv_end_pair - key0;
+                if (j == nt - 1) {
+                    const int tile0 = j * kChunkKeys;
+                    const int first = d.kv_end - tile0;
                     const int stop =
-                        min(kChunkKeys, ((kv_end_pair + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE) * PKV_BLOCK_SIZE - key0);
+                        min(kChunkKeys, ((d.kv_end + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE) * PKV_BLOCK_SIZE - tile0);
                     if (first < stop) {
-                        const uint32_t x = jt + j;
-                        const int st = x % kStages;
-                        if (!warp_wait(&v_full[st], (x / kStages) & 1, status, abort)) { ok = false; break; }
+                        const int st = x % kVStages;
+                        if (!warp_wait(&v_full[st], (x / kVStages) & 1, status, abort)) { ok = false; break; }
                         uint8_t *vt = smem + S::kOffV + st * S::kTile;
                         const int per_row = (D / 64) * 8;  // 16-byte chunks per V row
-                        for (int c = q4 * 32 + lane; c < (stop - first) * per_row; c += 128) {
+                        for (int c = warp * 32 + lane; c < (stop - first) * per_row; c += kSoftmaxWarps * 32) {
                             const int vr = first + c / per_row, rem = c % per_row;
-                            *reinterpret_cast<uint4 *>(vt + (rem / 8) * S::kHalf + vr * 128 + (rem % 8) * 16) =
-                                make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(vt + (vr / 16) * S::kBlk + (rem / 8) * 2048 + (vr % 16) * 128 +
+                                                       (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                     }
@@ -514,37 +525,38 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 tmem_wait_st();
                 tmem_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[t]);
+                if (lane == 0) mbar_arrive(&p_full[x & 1]);
             }
             jt += nt;
             if (!ok) break;
-            if (nt_mine == 0) continue;
-            // Output: O_t / l for the valid rows.
-            if (!warp_wait(&o_done[t], n_done & 1, status, abort)) break;
+            // Output: O / l for the valid rows, this warp's D / 4 columns.
+            float l_row;
+            if (!exchange(l, false, l_row)) break;
+            if (!warp_wait(o_done, n_done & 1, status, abort)) break;
             ++n_done;
             tmem_fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *dst = a.out + (out_row0 + (long long)i * a.num_q_heads + rho % g) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(o_col + c * 32, o);
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            __nv_bfloat16 *dst =
+                a.out + (((long long)d.q0 + i) * a.num_q_heads + d.h * g + rho % g) * D + part * kOCols;
+            {
+                float o[kOCols];
+                tmem_ld_cols(o_col, o);
                 tmem_wait_ld_regs(o);
                 if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
+                    for (int e = 0; e < kOCols; e += 8) {
                         uint4 pk;
                         pk.x = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
                         pk.y = pack_bf16x2(o[e + 2] * inv, o[e + 3] * inv);
                         pk.z = pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv);
                         pk.w = pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv);
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + e) = pk;
+                        *reinterpret_cast<uint4 *>(dst + e) = pk;
                     }
                 }
             }
             tmem_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[t]);
+            if (lane == 0) mbar_arrive(o_free);
         }
     }
 

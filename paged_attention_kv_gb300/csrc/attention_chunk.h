@@ -11,8 +11,8 @@
 
 namespace pkv {
 
-// a = {r, tile pair (256 rows), kv head h, keys seen by the pair's last row},
-// b = {qstart, n, L, valid rows of the pair}.
+// a = {r, 128-row tile mt, kv head h, keys seen by the tile's last row},
+// b = {qstart, n, L, valid rows of the tile}.
 struct ChunkItem {
     int4 a, b;
 };

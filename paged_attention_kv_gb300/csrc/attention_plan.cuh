@@ -56,11 +56,9 @@ constexpr int kCascadeMinReqs = 4;
 constexpr int kCascadeMaxBlocks = 4096;
 
 // Chunk tiles (tcgen05 path): requests with at least kChunkRows query rows
-// (n * g) are cut into 128-row tiles that run over 128-key tiles; one work
-// item takes two consecutive tiles of a request (kChunkPairRows rows), which
-// share one K/V stream.
+// (n * g) are cut into 128-row tiles that run over 128-key tiles; a work
+// item is one tile of one request and kv head.
 constexpr int kChunkRows = 128;
-constexpr int kChunkPairRows = 2 * kChunkRows;
 constexpr int kChunkKeys = 128;
 
 struct WsHeader {

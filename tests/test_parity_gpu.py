@@ -333,11 +333,10 @@ def test_host_step_pipeline_matches_device_steps(workload):
 
 
 @pytest.mark.parametrize("shape", [TINY, LLAMA], ids=["d64", "d128"])
-def test_chunk_pairs_with_and_without_a_second_tile(shape):
-    """Chunk work items hold two 128-row tiles of a request; a request whose
-    rows end on an odd tile leaves the last item with tile A only, and a
-    pair whose tiles see different numbers of 128-key tiles shares one K/V
-    stream."""
+def test_chunk_tiles_with_ragged_key_ranges(shape):
+    """Each 128-row chunk tile is one work item with its own key range:
+    requests of 1, 3, 5 and 2 tiles whose tiles end inside a 128-key tile,
+    at a block boundary and past several key tiles of prior context."""
     g = shape.num_q_heads // shape.num_kv_heads
     t = 128 // g  # tokens per 128-row tile
     ql = [t, 3 * t, 5 * t, 2 * t, 1]
