@@ -383,15 +383,20 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
         uint32_t jt = 0;      // key tiles of the items so far (global tile index base)
         uint32_t n_done = 0;  // items finished
         uint32_t n_x = 0;     // exchanges so far (the same sequence in the quadrant's four warps)
-        // The four part warps of this quadrant pool one float per row: the
-        // result is the same in all four (same values, same order).
-        auto exchange = [&](float v, bool is_max, float &res) -> bool {
-            const int par = n_x & 1;
-            float *xb = xbuf + par * (kParts * kChunkRows);
-            xb[part * kChunkRows + row] = v;
+        // The four part warps of this quadrant pool one float per row:
+        // publish, then (maybe after other work) collect; the result is the
+        // same in all four (same values, same order). A warp publishes
+        // exchange n + 2 into the slot of n only after collecting n + 1,
+        // which every warp published after collecting n.
+        auto publish = [&](float v) {
+            xbuf[(n_x & 1) * (kParts * kChunkRows) + part * kChunkRows + row] = v;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar[q4 * 2 + par]);
+            if (lane == 0) mbar_arrive(&xbar[q4 * 2 + (n_x & 1)]);
+        };
+        auto collect = [&](bool is_max, float &res) -> bool {
+            const int par = n_x & 1;
             if (!warp_wait(&xbar[q4 * 2 + par], (n_x >> 1) & 1, status, abort)) return false;
+            const float *xb = xbuf + par * (kParts * kChunkRows);
             float r = xb[row];
 #pragma unroll
             for (int p = 1; p < kParts; ++p) r = is_max ? fmaxf(r, xb[p * kChunkRows + row]) : r + xb[p * kChunkRows + row];
@@ -427,8 +432,34 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 float sv[kPartKeys];
                 tmem_ld32(s_col, sv);
                 tmem_wait_ld_regs(sv);
-                // Partial row max (scaled, masked), then the row's.
-                float mx;
+                // This part's P = 2^(s * scale - m) as bf16 pairs (32 keys ->
+                // 16 columns); returns the sum of the unrounded values.
+                auto compute_p = [&](const float (&sv)[kPartKeys], float neg_m, uint32_t (&pk)[kPartKeys / 2]) {
+                    if (fast) {
+                        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
+                        float2 la2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                        for (int e = 0; e < kPartKeys / 2; ++e) {
+                            const float2 xv = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), sc2, nm2);
+                            const float2 p = make_float2(fast_exp2(xv.x), fast_exp2(xv.y));
+                            la2[e & 1] = fadd2(la2[e & 1], p);
+                            pk[e] = pack_bf16x2(p.x, p.y);
+                        }
+                        return (la2[0].x + la2[0].y) + (la2[1].x + la2[1].y);
+                    }
+                    float la[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < kPartKeys / 2; ++e) {
+                        const int kk = key0 + (e / 4) * 16 + (2 * e) % 8;
+                        const float p0 = kk <= limit ? fast_exp2(fmaf(sv[2 * e], a.scale_log2, neg_m)) : 0.f;
+                        const float p1 = kk + 1 <= limit ? fast_exp2(fmaf(sv[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
+                        la[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    return (la[0] + la[1]) + (la[2] + la[3]);
+                };
+                // Partial row max (scaled, masked), published to the other
+                // three parts of the row.
                 {
                     float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     if (fast) {
@@ -443,52 +474,48 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                     }
                     float pm = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
                     if (fast) pm *= a.scale_log2;
-                    if (!exchange(pm, true, mx)) { ok = false; break; }
+                    publish(pm);
                 }
                 // The reference max moves only when the row max outgrows it by
-                // more than 2^8 (and on the first tile: key 0 is visible to
-                // every row, so mx is finite there).
-                const bool resc = j == 0 || mx > m_run + kRescaleThreshold;
-                const float alpha = (j > 0 && resc) ? fast_exp2(m_run - mx) : 1.f;
-                if (resc) m_run = mx;
-                const bool any_resc = j > 0 && __any_sync(0xffffffffu, resc);
+                // more than 2^8. The first tile sets it (key 0 is visible to
+                // every row, so the row max is finite there); later tiles
+                // compute P against the current reference while the partial
+                // maxima meet, and redo it in the rare case the row max
+                // moved the reference.
+                float mx;
+                if (j == 0) {
+                    if (!collect(true, mx)) { ok = false; break; }
+                    m_run = mx;
+                }
+                uint32_t pk[kPartKeys / 2];
+                float sum = compute_p(sv, -m_run, pk);
+                float alpha = 1.f;
+                bool any_resc = false;
+                if (j > 0) {
+                    if (!collect(true, mx)) { ok = false; break; }
+                    const bool resc = mx > m_run + kRescaleThreshold;
+                    any_resc = __any_sync(0xffffffffu, resc);
+                    if (any_resc) {
+                        if (resc) {
+                            alpha = fast_exp2(m_run - mx);
+                            m_run = mx;
+                        }
+                        // S(x) is still in TMEM: its buffer is rewritten only
+                        // after PV(x), which waits for this P.
+                        float sv2[kPartKeys];
+                        tmem_ld32(s_col, sv2);
+                        tmem_wait_ld_regs(sv2);
+                        sum = compute_p(sv2, -m_run, pk);
+                    }
+                }
                 // The P buffer of x was last read by PV(x-2).
                 if (x >= 2) {
                     const uint32_t y = x - 2;
                     if (!warp_wait(&pv_done[y & 1], (y >> 1) & 1, status, abort)) { ok = false; break; }
                     tmem_fence_after_sync();
                 }
-                // P = 2^(s * scale - m_run) as bf16 pairs (32 keys -> 16 columns).
-                {
-                    const float neg_m = -m_run;
-                    uint32_t pk[kPartKeys / 2];
-                    float sum;
-                    if (fast) {
-                        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
-                        float2 la2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                        for (int e = 0; e < kPartKeys / 2; ++e) {
-                            const float2 xv = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), sc2, nm2);
-                            const float2 p = make_float2(fast_exp2(xv.x), fast_exp2(xv.y));
-                            la2[e & 1] = fadd2(la2[e & 1], p);
-                            pk[e] = pack_bf16x2(p.x, p.y);
-                        }
-                        sum = (la2[0].x + la2[0].y) + (la2[1].x + la2[1].y);
-                    } else {
-                        float la[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int e = 0; e < kPartKeys / 2; ++e) {
-                            const int kk = key0 + (e / 4) * 16 + (2 * e) % 8;
-                            const float p0 = kk <= limit ? fast_exp2(fmaf(sv[2 * e], a.scale_log2, neg_m)) : 0.f;
-                            const float p1 = kk + 1 <= limit ? fast_exp2(fmaf(sv[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
-                            la[e & 3] += p0 + p1;
-                            pk[e] = pack_bf16x2(p0, p1);
-                        }
-                        sum = (la[0] + la[1]) + (la[2] + la[3]);
-                    }
-                    tmem_st16u(p_col, pk);
-                    l = fmaf(l, alpha, sum);
-                }
+                tmem_st16u(p_col, pk);
+                l = fmaf(l, alpha, sum);
                 // O (this warp's columns) follows a moved reference once
                 // PV(x-1) is done, before PV(x) is issued.
                 if (any_resc) {
@@ -531,7 +558,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
             if (!ok) break;
             // Output: O / l for the valid rows, this warp's D / 4 columns.
             float l_row;
-            if (!exchange(l, false, l_row)) break;
+            publish(l);
+            if (!collect(false, l_row)) break;
             if (!warp_wait(o_done, n_done & 1, status, abort)) break;
             ++n_done;
             tmem_fence_after_sync();

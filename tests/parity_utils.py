@@ -38,9 +38,16 @@ def attention_errors(got_bf16: torch.Tensor, ref: np.ndarray, rows=None):
     return float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0, rms, got
 
 
-def assert_attention_close(got_bf16, ref, rows=None, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what=""):
+def assert_attention_close(got_bf16, ref, rows=None, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what="", rel=0.0):
+    """Element-wise |got - ref| <= max_abs + rel * |ref| and mean-abs <= mean_abs.
+    rel is 0 for the workloads' bar; peaked inputs whose outputs approach
+    single V values (|O| of several units) add the bf16 terms that scale
+    with |O|."""
     mx, mn, rms, got = attention_errors(got_bf16, ref, rows)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
+    if rel:
+        excess = np.abs(got - ref) - rel * np.abs(ref)
+        mx = float(excess.max()) if excess.size else 0.0
     assert mx <= max_abs and mn <= mean_abs, f"{what}: max-abs {mx:.3e} mean-abs {mn:.3e} (ref rms {rms:.3e})"
     return mx, mn
 
