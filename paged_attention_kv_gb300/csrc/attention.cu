@@ -1139,6 +1139,25 @@ int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &
     return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
 }
 
+// The pool as the chunk kernel stages it: a 5-D map {64 columns, token
+// within an 8-token half, 64-column half, 8-token group of the block's rows
+// ((kv * Hkv + head) * 2 + token half), block}; one box is a whole (block, K
+// or V, head), landing as [token half][D / 64][8 tokens][128 B] (128-byte
+// swizzle). The 8-token groups of consecutive blocks are then evenly spaced,
+// so one N=128 tensor-core product covers a 128-key tile.
+int encode_kv_map_chunk(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &d) {
+    const cuuint64_t groups_per_block = 2ull * d.num_kv_heads * 2;
+    const cuuint64_t row = (cuuint64_t)d.head_size * 2;
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)d.head_size / 64, groups_per_block, (cuuint64_t)d.num_blocks};
+    cuuint64_t strides[4] = {row, 128, 8 * row, groups_per_block * 8 * row};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)d.head_size / 64, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
+}
+
 // q [T][Hq][D] as a 3-D map; one box is the 128 rows of a chunk tile: 128/g
 // tokens x the g q heads of one kv head x 64 columns.
 int encode_q_map(CUtensorMap *map, const void *q, int num_tokens, int num_q_heads, int head_size, int group) {
@@ -1198,9 +1217,10 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     // The chunk kernel takes requests with >= 128 query rows when a 128-row
     // tile holds whole tokens.
     const bool chunk_ok = kChunkRows % group == 0 && (long long)num_tokens * group >= kChunkRows;
-    CUtensorMap q_map;
+    CUtensorMap q_map, kv_map_chunk;
     if (chunk_ok) {
         rc = encode_q_map(&q_map, q, num_tokens, num_q_heads, D, group);
+        if (!rc) rc = encode_kv_map_chunk(&kv_map_chunk, kv_cache, *desc);
         if (rc) return rc;
     }
 
@@ -1275,7 +1295,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.items = pa.chunk_items;
         ca.header = header;
         ca.out = static_cast<__nv_bfloat16 *>(out);
-        if (chunk_launch(D, di->sm_count, kv_map, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
+        if (chunk_launch(D, di->sm_count, kv_map_chunk, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     }
     record(events, 2, st);
     if (D == 128)

@@ -19,21 +19,20 @@
 //   O += P(x) V(x)    tcgen05.mma (M=128, N=D) with A = P(x) read from TMEM
 //                     and B = V MN-major straight from its TMA tile; O stays
 //                     in TMEM.
-// K and V tiles arrive one copy per block (16 keys x D), as D / 64 pieces of
-// [16 keys][64 columns]; the S product runs as two N=64 halves, tokens 0-7
-// of the eight blocks and tokens 8-15, so S, P and the PV product's K steps
-// see the tile's keys in the order (token half, block, token): column c <
-// 64 is key 16 * (c / 8) + c % 8, column c >= 64 key 16 * ((c - 64) / 8) +
-// 8 + c % 8. Masks follow the same order.
+// K and V tiles arrive one copy per block (16 keys x D; the copy engine
+// spends a fixed cost per box, so one box per block rather than per 64
+// columns), laid out [token half][D / 64][8 tokens][128 B]: the tile's 16
+// groups of 8 keys are evenly spaced, so S is one N=128 product per K step
+// and the PV product's K steps are single blocks.
 // The softmax of tile x waits only for S(x) and for the P buffer of tile x-2
 // to be consumed; the tensor core runs PV(x-1) and S(x+1) meanwhile. One
 // warp per row would leave each SM sub-partition a single long dependency
 // chain per tile; four shorter ones interleave. Warps: 0-15 softmax and
 // output (warp w: lane quadrant w % 4, key part w / 4), 16 TMA producer (Q
-// tile; K and V tiles of 8 blocks, one box per 64 columns of each block; K
-// runs a tile ahead of V), 17 MMA issuer (one elected lane) and TMEM owner. Every wait is bounded; on a
-// timeout the CTA raises PKV_DEV_TIMEOUT, stops, lets its in-flight copies
-// and MMAs finish and frees its TMEM.
+// tile; K and V tiles of 8 blocks; K runs a tile ahead of V), 17 MMA issuer
+// (one elected lane) and TMEM owner. Every wait is bounded; on a timeout the
+// CTA raises PKV_DEV_TIMEOUT, stops, lets its in-flight copies and MMAs
+// finish and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -52,7 +51,6 @@ namespace {
 constexpr int kParts = 4;                          // softmax warps per TMEM lane quadrant
 constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kPartKeys = kChunkKeys / kParts;     // keys of one warp's part
-static_assert(kParts == 4 && kChunkKeys == 128, "the key order assumes four 32-key parts of a 128-key tile");
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kChunkThreads = 32 * (kSoftmaxWarps + 2);
 // TMEM columns: S0 | S1 (fp32, 128 each) | P0 | P1 (bf16 pairs, 64 each) | O (D).
@@ -95,7 +93,8 @@ struct ChunkSmem {
     using Bars = ChunkBars<kKStages, kVStages>;
     static constexpr int kHalf = 16384;             // Q: 128 rows x 128 B (64 bf16 columns)
     static constexpr int kTile = (D / 64) * kHalf;  // 128 rows x D bf16
-    static constexpr int kBlk = (D / 64) * 2048;    // K / V: one block [D / 64][16 keys][128 B]
+    static constexpr int kGrp = (D / 64) * 1024;    // K / V: 8 keys of one block [D / 64][8][128 B]
+    static constexpr int kBlk = 2 * kGrp;           // one block: two 8-key groups
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTile;
     static constexpr int kOffV = kOffK + kKStages * kTile;
@@ -252,7 +251,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 __syncwarp();
                 if (lane < kTileBlocks) {
                     uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * S::kBlk;
-                    tma_load_4d(dst, &kv_map, 0, (is_v ? Hkv + h : h) * PKV_BLOCK_SIZE, 0, blk, full);
+                    tma_load_5d(dst, &kv_map, 0, 0, 0, (is_v ? Hkv + h : h) * 2, blk, full);
                 }
                 __syncwarp();
                 if (is_v) ++v_issued; else ++k_issued;
@@ -290,29 +289,24 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
         // The whole warp walks the schedule with the same values (so
         // descriptors and TMEM addresses stay warp-uniform); one elected lane
         // issues every tcgen05.mma and commit.
-        constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys / 2, 0, 0);
+        constexpr uint32_t kIdS = umma_idesc_bf16(128, kChunkKeys, 0, 0);
         constexpr uint32_t kIdPV = umma_idesc_bf16(128, D, 0, 1);
         const uint32_t q_s = smem_u32(smem + S::kOffQ);
         const uint32_t k_s = smem_u32(smem + S::kOffK), v_s = smem_u32(smem + S::kOffV);
         uint32_t jt = 0;  // key tiles of the items so far (global tile index base)
         uint32_t n_items_done = 0;
         bool ok = true;
-        // S(x) = Q K(x)^T into S buffer x & 1, as two N=64 products: tokens
-        // 0-7 of the eight blocks (8-row groups one block apart), then tokens
-        // 8-15. Its K slot is released when the product is done (it is the
-        // slot's only reader).
+        // S(x) = Q K(x)^T into S buffer x & 1 (the key tile's 8-key groups
+        // kGrp bytes apart). Its K slot is released when the product is done
+        // (it is the slot's only reader).
         auto issue_s = [&](uint32_t x) {
             const int st = x % kKStages;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t qd = umma_desc_sw128(q_s + (kk / 4) * S::kHalf + (kk % 4) * 32, 16, 1024);
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr)
-                    umma_bf16_warp(tm + (x & 1) * kChunkKeys + hr * (kChunkKeys / 2), qd,
-                                   umma_desc_sw128(k_s + st * S::kTile + (kk / 4) * 2048 + (kk % 4) * 32 + hr * 1024,
-                                                   16, S::kBlk),
-                                   kIdS, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_warp(tm + (x & 1) * kChunkKeys,
+                               umma_desc_sw128(q_s + (kk / 4) * S::kHalf + (kk % 4) * 32, 16, 1024),
+                               umma_desc_sw128(k_s + st * S::kTile + (kk / 4) * 1024 + (kk % 4) * 32, 16, S::kGrp),
+                               kIdS, kk > 0 ? 1u : 0u);
             umma_commit_warp(&s_full[x & 1]);
             umma_commit_warp(&k_empty[st]);
         };
@@ -343,12 +337,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 if (!warp_wait(&v_full[st], (x / kVStages) & 1, status, abort)) { ok = false; break; }
                 tmem_fence_after_sync();
                 // O += P(x) V(x): P from TMEM (64 columns of bf16 pairs), V
-                // MN-major; K step kk takes tokens 0-7 (kk < 4) or 8-15 of
-                // blocks 2 (kk % 4) and 2 (kk % 4) + 1, as S ordered them.
+                // MN-major; K step kk is block kk (its two 8-key groups kGrp
+                // apart, its 64-column halves 1 KiB apart).
 #pragma unroll
                 for (int kk = 0; kk < kChunkKeys / 16; ++kk) {
-                    const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + (kk % 4) * 2 * S::kBlk + (kk / 4) * 1024,
-                                                        2048, S::kBlk);
+                    const uint64_t bd = umma_desc_sw128(v_s + st * S::kTile + kk * S::kBlk, 1024, S::kGrp);
                     umma_bf16_tmem_a_warp(tm + kColO, tm + kColP + (x & 1) * 64 + kk * 8, bd, kIdPV,
                                           (j > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -423,12 +416,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 const uint32_t p_col = tm + lane_off + kColP + (x & 1) * 64 + part * (kPartKeys / 2);
                 if (!warp_wait(&s_full[x & 1], (x >> 1) & 1, status, abort)) { ok = false; break; }
                 tmem_fence_after_sync();
-                // This part's column e holds key key0 + 16 * (e / 8) + e % 8.
-                const int key0 = j * kChunkKeys + (part & 1) * (kChunkKeys / 2) + (part >> 1) * 8;
+                const int key0 = j * kChunkKeys + part * kPartKeys;  // first key of this part
                 // Parts the whole warp sees unmasked take a path without
                 // per-key tests; with a positive scale the max can be taken
                 // on the raw scores.
-                const bool fast = __all_sync(0xffffffffu, key0 + 55 <= limit) && a.scale_log2 > 0.f;
+                const bool fast = __all_sync(0xffffffffu, key0 + kPartKeys - 1 <= limit) && a.scale_log2 > 0.f;
                 float sv[kPartKeys];
                 tmem_ld32(s_col, sv);
                 tmem_wait_ld_regs(sv);
@@ -450,7 +442,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                     float la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int e = 0; e < kPartKeys / 2; ++e) {
-                        const int kk = key0 + (e / 4) * 16 + (2 * e) % 8;
+                        const int kk = key0 + 2 * e;
                         const float p0 = kk <= limit ? fast_exp2(fmaf(sv[2 * e], a.scale_log2, neg_m)) : 0.f;
                         const float p1 = kk + 1 <= limit ? fast_exp2(fmaf(sv[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
                         la[e & 3] += p0 + p1;
@@ -469,8 +461,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                     } else {
 #pragma unroll
                         for (int e = 0; e < kPartKeys; ++e)
-                            mxa[e & 3] = fmaxf(mxa[e & 3], key0 + (e / 8) * 16 + e % 8 <= limit ? sv[e] * a.scale_log2
-                                                                                                : -INFINITY);
+                            mxa[e & 3] = fmaxf(mxa[e & 3], key0 + e <= limit ? sv[e] * a.scale_log2 : -INFINITY);
                     }
                     float pm = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
                     if (fast) pm *= a.scale_log2;
@@ -543,7 +534,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                         const int per_row = (D / 64) * 8;  // 16-byte chunks per V row
                         for (int c = warp * 32 + lane; c < (stop - first) * per_row; c += kSoftmaxWarps * 32) {
                             const int vr = first + c / per_row, rem = c % per_row;
-                            *reinterpret_cast<uint4 *>(vt + (vr / 16) * S::kBlk + (rem / 8) * 2048 + (vr % 16) * 128 +
+                            *reinterpret_cast<uint4 *>(vt + (vr / 8) * S::kGrp + (rem / 8) * 1024 + (vr % 8) * 128 +
                                                        (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();

@@ -141,6 +141,16 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// 5-D tiled bulk-tensor load into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(void *smem_dst, const void *tmap, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, int32_t c4, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---- programmatic dependent launch ----------------------------------------
 
 // Lets the next kernel on the stream (launched with programmatic stream
