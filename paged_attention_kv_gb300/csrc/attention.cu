@@ -688,8 +688,7 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
             if (lane == 0) {
                 uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
                 mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-                tma_load_4d(st, kv_map, 0, h * PKV_BLOCK_SIZE, 0, blk, &full[stage]);
-                tma_load_4d(st + S::kTileBytes, kv_map, 0, (Hkv + h) * PKV_BLOCK_SIZE, 0, blk, &full[stage]);
+                tma_load_5d(st, kv_map, 0, h * PKV_BLOCK_SIZE, 0, 0, blk, &full[stage]);
             }
             __syncwarp();
             ++e;
@@ -1121,19 +1120,20 @@ long long default_part_rows_cap(int sm_count, long long num_tokens, int num_q_he
     return max(grid_rows, prefix_rows);
 }
 
-// The pool [NB][2][Hkv][16][D] as a 4-D map {64 columns, row of the block
-// (kv * Hkv + head) * 16 + token, 64-column half, block}; one box is a whole
-// (block, K or V, head): 16 rows x D columns, landing in shared memory as
-// D / 64 consecutive 2 KiB pieces [half][16 rows][128 B] (128-byte swizzle).
-// One copy per block and head instead of one per 64 columns: the copy engine
-// spends a fixed cost per box.
+// The pool [NB][2][Hkv][16][D] as a 5-D map {64 columns, row of the head
+// (head * 16 + token), 64-column half, K or V, block}; one box is a whole
+// (block, head): its 16 K rows and 16 V rows x D columns, landing in shared
+// memory as [K / V][D / 64][16 rows][128 B] (128-byte swizzle). One copy per
+// block and head instead of one per 64 columns of K and of V: the copy
+// engine spends a fixed cost per box.
 int encode_kv_map(CUtensorMap *map, const void *kv_cache, const pkv_cache_desc &d) {
-    const cuuint64_t rows_per_block = 2ull * d.num_kv_heads * PKV_BLOCK_SIZE;
-    cuuint64_t dims[4] = {64, rows_per_block, (cuuint64_t)d.head_size / 64, (cuuint64_t)d.num_blocks};
-    cuuint64_t strides[3] = {(cuuint64_t)d.head_size * 2, 128, rows_per_block * d.head_size * 2};
-    cuuint32_t box[4] = {64, PKV_BLOCK_SIZE, (cuuint32_t)d.head_size / 64, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv_cache), dims, strides,
+    const cuuint64_t rows_per_kv = (cuuint64_t)d.num_kv_heads * PKV_BLOCK_SIZE;
+    const cuuint64_t row = (cuuint64_t)d.head_size * 2;
+    cuuint64_t dims[5] = {64, rows_per_kv, (cuuint64_t)d.head_size / 64, 2, (cuuint64_t)d.num_blocks};
+    cuuint64_t strides[4] = {row, 128, rows_per_kv * row, 2 * rows_per_kv * row};
+    cuuint32_t box[5] = {64, PKV_BLOCK_SIZE, (cuuint32_t)d.head_size / 64, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
