@@ -440,7 +440,8 @@ def main():
                                batch.num_blocks, b.slot_mapping, b.status)
         pkv.paged_kv_write(b.k, b.v, b.slot_mapping, b.kv_cache, b.status)
         pkv.paged_attention(b.q, b.kv_cache, b.block_table, b.seq_lens, b.query_start_loc, batch.scale,
-                            b.out, b.workspace, events=ev[i] if timed_kernels else None)
+                            b.out, b.workspace, events=ev[i] if timed_kernels else None,
+                            max_query_len=b.max_query_len)
 
     scrub = torch.empty(L2_SCRUB_BYTES, dtype=torch.uint8, device=dev) if mode == "flush" else None
     sampler = ClockSampler(local_rank)

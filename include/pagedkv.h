@@ -226,6 +226,25 @@ int paged_attention_timed(const void *q, int32_t num_tokens, int32_t num_q_heads
                           void *const *events);
 
 /*
+ * paged_attention with a caller bound on new tokens per request, as an
+ * engine's scheduler knows it for each step (the pages' attention metadata
+ * carries the longest query of the batch): max_query_len >= every request's
+ * query_start_loc[r + 1] - query_start_loc[r], or 0 for no bound. When
+ * max_query_len x (num_q_heads / num_kv_heads) < 128 no request can fill a
+ * 128-row chunk tile, and the chunk-tile kernel is not launched at all (a
+ * decode-only step saves that launch). A bound that is too small is not
+ * detected and stays correct: every row then takes the split-KV path.
+ * events: NULL, or four cudaEvent_t handles as for paged_attention_timed.
+ * Other arguments, results and errors as paged_attention.
+ */
+int paged_attention_bounded(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                            const void *kv_cache, const pkv_cache_desc *desc,
+                            const int32_t *block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                            const int32_t *seq_lens, const int32_t *query_start_loc, int32_t max_query_len,
+                            float scale, void *out, void *workspace, size_t workspace_bytes, void *stream,
+                            void *const *events);
+
+/*
  * paged_attention without a workspace argument, for callers that cannot
  * allocate device memory at the point where they run attention: an engine
  * that has already given nearly all free device memory to its KV pool (the

@@ -40,7 +40,7 @@ PKV_DEV_OVERFLOW = 0x20
 EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_gather_blocks",
             "paged_kv_scatter_blocks", "paged_attention_workspace_bytes",
             "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
-            "paged_attention_static", "pkv_read_status", "pkv_selftest_bounded_wait", "pkv_status_string")
+            "paged_attention_bounded", "paged_attention_static", "pkv_read_status", "pkv_selftest_bounded_wait", "pkv_status_string")
 
 
 class PagedKVError(RuntimeError):
@@ -69,6 +69,8 @@ def _load():
     lib.paged_attention_min_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
     lib.paged_attention.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     lib.paged_attention_timed.argtypes = lib.paged_attention.argtypes + [ctypes.POINTER(vp)]
+    lib.paged_attention_bounded.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, i32, ctypes.c_float, vp,
+                                            vp, sz, vp, ctypes.POINTER(vp)]
     lib.paged_attention_static.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp]
     lib.pkv_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
     lib.pkv_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -224,11 +226,12 @@ def alloc_workspace(max_num_reqs: int, max_num_tokens: int, num_q_heads: int, kv
 
 
 def paged_attention(q, kv_cache, block_table, seq_lens, query_start_loc, scale: float, out=None, workspace=None,
-                    stream=None, events=None) -> torch.Tensor:
+                    stream=None, events=None, max_query_len: int = 0) -> torch.Tensor:
     """Attention over the paged pool. ``events``: optional four
     torch.cuda.Event(enable_timing=True) recorded before the work-list
     kernel, after it, after the chunk-tile kernel and after the split-KV
-    kernel."""
+    kernel. ``max_query_len``: optional bound on any request's new tokens
+    (0: none); below 128 / GQA group the chunk-tile kernel is not launched."""
     _want(q, torch.bfloat16, 3, "q")
     _want(kv_cache, torch.bfloat16, 5, "kv_cache")
     _want(block_table, torch.int32, 2, "block_table")
@@ -253,7 +256,13 @@ def paged_attention(q, kv_cache, block_table, seq_lens, query_start_loc, scale: 
     nbytes = workspace.numel() * workspace.element_size()
     args = (_ptr(q), t, hq, _ptr(kv_cache), ctypes.byref(desc), _ptr(block_table), num_reqs, block_table.shape[1],
             _ptr(seq_lens), _ptr(query_start_loc), float(scale), _ptr(out), _ptr(workspace), nbytes, _stream(stream))
-    if events is None:
+    if max_query_len:
+        head, tail = args[:10], args[10:]
+        handles = None
+        if events is not None:
+            handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(_event_handle(e, stream)) for e in events])
+        _check(LIB.paged_attention_bounded(*head, int(max_query_len), *tail, handles), "paged_attention_bounded")
+    elif events is None:
         _check(LIB.paged_attention(*args), "paged_attention")
     else:
         handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(_event_handle(e, stream)) for e in events])
@@ -324,6 +333,8 @@ class StepBuffers:
         self.seq_lens = torch.from_numpy(batch.seq_lens).to(dev)
         self.query_start_loc = torch.from_numpy(batch.query_start_loc).to(dev)
         self.num_tokens = batch.num_tokens
+        # the longest request's new tokens, known to the scheduler that built the batch
+        self.max_query_len = int(batch.query_lens.max()) if batch.num_reqs else 0
         self.slot_mapping = torch.empty(self.num_tokens, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
@@ -335,7 +346,7 @@ class StepBuffers:
                            self.batch.num_blocks, self.slot_mapping, self.status, stream)
         paged_kv_write(self.k, self.v, self.slot_mapping, self.kv_cache, self.status, stream)
         paged_attention(self.q, self.kv_cache, self.block_table, self.seq_lens, self.query_start_loc,
-                        self.batch.scale, self.out, self.workspace, stream)
+                        self.batch.scale, self.out, self.workspace, stream, max_query_len=self.max_query_len)
         return self.out
 
 
@@ -447,12 +458,15 @@ class HostStepPipeline:
             self.loaded[b].synchronize()  # the slot's previous copy has been read
         return self.host_in[b]
 
-    def submit(self, out_host: torch.Tensor, num_reqs: int | None = None, kv_cache=None) -> torch.cuda.Event:
+    def submit(self, out_host: torch.Tensor, num_reqs: int | None = None, kv_cache=None,
+               max_query_len: int | None = None) -> torch.cuda.Event:
         """Enqueue the step whose inputs are in ``next_inputs()``; returns the
         event after which ``out_host`` holds its output. ``num_reqs``: the
         requests of this step (default: all). ``kv_cache``: this step's pool
         when it is not the one the pipeline was built with (another layer's
-        pool of the same shape)."""
+        pool of the same shape). ``max_query_len``: the longest request of
+        the step, as the scheduler knows it (default: taken from the host
+        copy of query_start_loc; 0: unknown)."""
         pool = self.kv_cache if kv_cache is None else kv_cache
         if pool.shape != self.kv_cache.shape or pool.dtype != self.kv_cache.dtype:
             raise PagedKVError(PKV_E_DIMS, "kv_cache differs in shape from the pipeline's pool")
@@ -461,6 +475,9 @@ class HostStepPipeline:
             raise PagedKVError(PKV_E_DIMS, "num_reqs outside the pipeline's bounds")
         b = self.i % self.depth
         din = self.dev_in[b]
+        if max_query_len is None:
+            hq = self.host_in[b]["query_start_loc"][:R + 1]
+            max_query_len = int((hq[1:] - hq[:-1]).max())
         with torch.cuda.stream(self.h2d):
             if self.used[b]:
                 self.h2d.wait_event(self.computed[b])  # the step that last read this slot is done
@@ -473,7 +490,8 @@ class HostStepPipeline:
         paged_slot_mapping(bt, sl, qsl, self.num_tokens, self.num_blocks, self.slot_mapping[b], self.status,
                            self.compute)
         paged_kv_write(din["k"], din["v"], self.slot_mapping[b], pool, self.status, self.compute)
-        paged_attention(din["q"], pool, bt, sl, qsl, self.scale, self.out[b], self.workspace, self.compute)
+        paged_attention(din["q"], pool, bt, sl, qsl, self.scale, self.out[b], self.workspace, self.compute,
+                        max_query_len=max(0, max_query_len))
         self.computed[b].record(self.compute)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.computed[b])

@@ -1178,7 +1178,8 @@ void record(void *const *events, int i, cudaStream_t st) {
 int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const void *kv_cache,
                    const pkv_cache_desc *desc, const int32_t *block_table, int32_t num_reqs,
                    int32_t max_blocks_per_req, const int32_t *seq_lens, const int32_t *query_start_loc, float scale,
-                   void *out, void *workspace, size_t workspace_bytes, void *stream, void *const *events) {
+                   void *out, void *workspace, size_t workspace_bytes, void *stream, void *const *events,
+                   int32_t max_query_len) {
     if (!desc) return PKV_E_NULL;
     int rc = check_cache_desc(*desc, /*attention=*/true);
     if (rc) return rc;
@@ -1216,7 +1217,12 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     const int group = num_q_heads / Hkv;
     // The chunk kernel takes requests with >= 128 query rows when a 128-row
     // tile holds whole tokens.
-    const bool chunk_ok = kChunkRows % group == 0 && (long long)num_tokens * group >= kChunkRows;
+    // A caller bound on new tokens per request (0: none) that keeps every
+    // request below 128 rows means no chunk tiles: the chunk kernel is not
+    // launched and the work list puts every row on the split-KV path (so a
+    // bound that is too small costs speed, never correctness).
+    const bool chunk_ok = kChunkRows % group == 0 && (long long)num_tokens * group >= kChunkRows &&
+                          (max_query_len <= 0 || (long long)max_query_len * group >= kChunkRows);
     CUtensorMap q_map, kv_map_chunk;
     if (chunk_ok) {
         rc = encode_q_map(&q_map, q, num_tokens, num_q_heads, D, group);
@@ -1346,7 +1352,19 @@ extern "C" PKV_API int paged_attention(const void *q, int32_t num_tokens, int32_
                                        const int32_t *query_start_loc, float scale, void *out, void *workspace,
                                        size_t workspace_bytes, void *stream) {
     return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
-                          seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, nullptr);
+                          seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+extern "C" PKV_API int paged_attention_bounded(const void *q, int32_t num_tokens, int32_t num_q_heads,
+                                               const void *kv_cache, const pkv_cache_desc *desc,
+                                               const int32_t *block_table, int32_t num_reqs,
+                                               int32_t max_blocks_per_req, const int32_t *seq_lens,
+                                               const int32_t *query_start_loc, int32_t max_query_len, float scale,
+                                               void *out, void *workspace, size_t workspace_bytes, void *stream,
+                                               void *const *events) {
+    return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
+                          seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, events,
+                          max_query_len);
 }
 
 extern "C" PKV_API int paged_attention_timed(const void *q, int32_t num_tokens, int32_t num_q_heads,
@@ -1356,7 +1374,7 @@ extern "C" PKV_API int paged_attention_timed(const void *q, int32_t num_tokens, 
                                              const int32_t *query_start_loc, float scale, void *out, void *workspace,
                                              size_t workspace_bytes, void *stream, void *const *events) {
     return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
-                          seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, events);
+                          seq_lens, query_start_loc, scale, out, workspace, workspace_bytes, stream, events, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1409,5 +1427,5 @@ extern "C" PKV_API int paged_attention_static(const void *q, int32_t num_tokens,
     const int rc = static_scratch_address(&scratch);
     if (rc) return rc;
     return attention_impl(q, num_tokens, num_q_heads, kv_cache, desc, block_table, num_reqs, max_blocks_per_req,
-                          seq_lens, query_start_loc, scale, out, scratch, kStaticScratchBytes, stream, nullptr);
+                          seq_lens, query_start_loc, scale, out, scratch, kStaticScratchBytes, stream, nullptr, 0);
 }

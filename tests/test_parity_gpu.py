@@ -371,6 +371,36 @@ def test_chunk_tiles_with_scores_growing_along_the_context():
     _check_full(batch, {key: val.to("cuda") for key, val in ten.items()}, rel=2.0 ** -7)
 
 
+def test_max_query_len_bound_skips_the_chunk_kernel_and_stays_correct():
+    """paged_attention_bounded: a decode batch gives the same bits with and
+    without the bound (the bound only drops the chunk kernel's launch); a
+    bound too small for the batch's chunk requests sends their rows down the
+    split-KV path, still within tolerance of the oracle."""
+    dec = _custom(LLAMA, [300, 1200, 47, 2000], [1, 1, 1, 1], 660)
+    ten = device_tensors(dec, generate_on="cpu")
+    buf = pkv.StepBuffers(dec, {k: v.clone() for k, v in ten.items()})
+    buf.step()
+    with_bound = buf.out.clone()
+    pkv.paged_attention(buf.q, buf.kv_cache, buf.block_table, buf.seq_lens, buf.query_start_loc, dec.scale,
+                        buf.out, buf.workspace)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(buf.workspace) == 0
+    assert torch.equal(with_bound.view(torch.int16), buf.out.view(torch.int16))
+
+    mixed = _custom(LLAMA, [700, 90, 1500], [200, 1, 64], 661)
+    ten = device_tensors(mixed, generate_on="cpu")
+    host = host_inputs(ten)
+    slots, pool, ref = oracle_step(mixed, host)
+    buf = pkv.StepBuffers(mixed, ten)
+    buf.max_query_len = 1  # too small: requests 0 and 2 have 800 and 256 rows
+    buf.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(buf.status) == 0 and pkv.pkv_read_status(buf.workspace) == 0
+    h = buf.workspace[:8].view(torch.int32).cpu().numpy()
+    assert int(h[6]) == 0  # no chunk items: every row went to the split-KV path
+    assert_attention_close(buf.out, ref, what="too-small bound")
+
+
 def test_a_wait_that_never_completes_is_reported_and_the_context_survives():
     """Failure detection without a fault: the self-test's wait on a barrier
     that nothing arrives on gives up after 2 ms, the status word carries
