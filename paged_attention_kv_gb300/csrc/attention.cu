@@ -698,6 +698,196 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
     return ok;
 }
 
+// One consumer warp's share of an item: its blocks (every kConsumerWarps-th
+// of [kb0, kb1)) against the item's NT * 8 query rows, then its unnormalised
+// O, running max and sum per row into the CTA's scratch for the combine.
+//
+// The products run transposed, with the query rows as the mma's N = 8
+// dimension: S^T (16 keys x 8 rows) = K Q^T and O^T (D x 8 rows) += V^T P^T.
+// An item with at most 8 valid rows (a decode token's GQA group up to 8)
+// then costs half the mma instructions of a 16-row tile; the legacy mma
+// path sets this kernel's per-block rate, which with 16-row products is
+// about the HBM rate itself. P^T goes from the accumulator layout to the B
+// operand layout with two 8x8 register transposes (movmatrix).
+template <int D, int NT>
+__device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem, const ItemDesc &d, int qb,
+                                             uint64_t *full, uint64_t *empty, uint32_t &e, int32_t *status,
+                                             volatile int *abort, int warp, int lane, float *scr, float2 *sml) {
+    using S = DecodeSmem<D>;
+    const int gid = lane >> 2, tig = lane & 3;  // fragment row group and column pair
+    const int mi = lane >> 3;                   // ldmatrix: which 8x8 matrix this lane addresses
+    // Per thread: rows r = nt * 8 + 2 tig + i (i = 0, 1) of each n-tile;
+    // O^T accumulators ot[dc][nt]: {d = 16 dc + gid, 16 dc + gid + 8} x
+    // {row 2 tig, 2 tig + 1}.
+    float ot[D / 16][NT][4];
+#pragma unroll
+    for (int dc = 0; dc < D / 16; ++dc)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) ot[dc][nt][0] = ot[dc][nt][1] = ot[dc][nt][2] = ot[dc][nt][3] = 0.f;
+    float m[NT][2], l[NT][2];
+    int lim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            m[nt][i] = -INFINITY;
+            l[nt][i] = 0.f;
+            lim[nt][i] = d.row_limit[nt * 8 + 2 * tig + i];
+        }
+
+    const int kb0 = d.kb0, kb1 = d.kb1, kv_end = d.kv_end;
+    // Q^T as the B operand of S^T, for the whole item: qf[kk][nt] = rows
+    // nt * 8 + gid, columns 16 kk + 2 tig (+ 8). Rows past n_valid hold stale
+    // data; they only affect their own rows, which are never written.
+    uint32_t qf[D / 16][NT][2];
+    {
+        const uint32_t qs = smem_u32(smem + S::kOffQ + qb * S::kQBytes);
+        const int row = (lane & 7) + ((mi >> 1) & 1) * 8;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(qs + row * S::kQStride + (16 * kk + (mi & 1) * 8) * 2, r0, r1, r2, r3);
+            qf[kk][0][0] = r0;
+            qf[kk][0][1] = r1;
+            if constexpr (NT == 2) {
+                qf[kk][NT - 1][0] = r2;
+                qf[kk][NT - 1][1] = r3;
+            }
+        }
+    }
+
+    for (int kb = kb0; kb < kb1; ++kb, ++e) {
+        if (((kb - kb0) & (kConsumerWarps - 1)) != warp) continue;
+        const int stage = e % S::kStages;
+        if (!mbar_wait(&full[stage], (e / S::kStages) & 1, status, abort)) break;
+        uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
+        const uint32_t kbase = smem_u32(st), vbase = kbase + S::kTileBytes;
+        const int key0 = kb * PKV_BLOCK_SIZE;
+
+        // Rows of V past the tile's last visible key may hold anything
+        // (other requests' stale data, NaN); their P is 0, but 0 * NaN is
+        // not, so clear them.
+        const bool tail = key0 + PKV_BLOCK_SIZE > kv_end;
+        if (tail) {
+            const int first = kv_end - key0;  // 1..15
+            for (int c = lane; c < (PKV_BLOCK_SIZE - first) * S::kBoxes * 8; c += 32) {
+                const int row = first + c / (S::kBoxes * 8);
+                const int rem = c % (S::kBoxes * 8);
+                *reinterpret_cast<uint4 *>(st + S::kTileBytes + (rem >> 3) * 2048 + row * 128 + (rem & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+
+        // S^T = K Q^T: A = the block's 16 keys x 16 columns per K step.
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        {
+            const int key = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int chunk = 2 * kk + (mi >> 1);
+                uint32_t ka[4];
+                ldmatrix_x4(kbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], ka, qf[kk][nt][0], qf[kk][nt][1]);
+            }
+        }
+
+        // Scale into the log2 domain, causal mask, online softmax per row
+        // (a column of S^T: keys gid and gid + 8 here, the rest across the
+        // lanes of equal tig).
+        uint32_t pb[NT][2];
+        float al[NT][2];
+        bool moved = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float mx[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float s0 = key0 + gid <= lim[nt][i] ? sc[nt][i] * a.scale_log2 : -INFINITY;
+                const float s1 = key0 + gid + 8 <= lim[nt][i] ? sc[nt][2 + i] * a.scale_log2 : -INFINITY;
+                sc[nt][i] = s0;
+                sc[nt][2 + i] = s1;
+                mx[i] = fmaxf(s0, s1);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 4));
+                mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 8));
+                mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 16));
+            }
+            float p[4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float mn = fmaxf(m[nt][i], mx[i]);
+                const float base = mn == -INFINITY ? 0.f : mn;
+                al[nt][i] = fast_exp2(m[nt][i] - base);
+                moved |= al[nt][i] != 1.f;
+                m[nt][i] = mn;
+                p[i] = fast_exp2(sc[nt][i] - base);
+                p[2 + i] = fast_exp2(sc[nt][2 + i] - base);
+                l[nt][i] = l[nt][i] * al[nt][i] + (p[i] + p[2 + i]);
+            }
+            // P^T (keys x rows) in the accumulator layout, as bf16 pairs,
+            // transposed into the B operand of O^T += V^T P^T.
+            pb[nt][0] = movmatrix_trans(pack_bf16x2(p[0], p[1]));  // keys 0-7
+            pb[nt][1] = movmatrix_trans(pack_bf16x2(p[2], p[3]));  // keys 8-15
+        }
+        if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+            for (int dc = 0; dc < D / 16; ++dc)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    ot[dc][nt][0] *= al[nt][0];
+                    ot[dc][nt][1] *= al[nt][1];
+                    ot[dc][nt][2] *= al[nt][0];
+                    ot[dc][nt][3] *= al[nt][1];
+                }
+        }
+
+        // O^T += V^T P^T: A = V^T, 16 columns x the block's 16 keys per step.
+        {
+            const int key = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int dc = 0; dc < D / 16; ++dc) {
+                const int chunk = 2 * dc + (mi & 1);
+                uint32_t va[4];
+                ldmatrix_x4_trans(vbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), va[0], va[1], va[2], va[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(ot[dc][nt], va, pb[nt][0], pb[nt][1]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            if (tail) fence_proxy_async_smem();
+            mbar_arrive(&empty[stage]);
+        }
+    }
+
+    // This warp's state per row -> scratch: sums over the lanes of equal
+    // tig, O^T transposed back into rows.
+    float *ws = scr + warp * kRowsPerTile * S::kScrStride;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float s = l[nt][i];
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            s += __shfl_xor_sync(0xffffffffu, s, 8);
+            s += __shfl_xor_sync(0xffffffffu, s, 16);
+            const int row = nt * 8 + 2 * tig + i;
+            if (gid == 0) sml[warp * kRowsPerTile + row] = make_float2(m[nt][i], s);
+#pragma unroll
+            for (int dc = 0; dc < D / 16; ++dc) {
+                ws[row * S::kScrStride + 16 * dc + gid] = ot[dc][nt][i];
+                ws[row * S::kScrStride + 16 * dc + gid + 8] = ot[dc][nt][2 + i];
+            }
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, D == 128 ? 2 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
@@ -775,8 +965,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
 
     // -------------------------------- consumers --------------------------------
     const int tid = threadIdx.x;  // 0..127
-    const int qrow = lane >> 2;   // fragment rows qrow and qrow + 8
-    const int qcol = (lane & 3) * 2;
     float *scr = reinterpret_cast<float *>(smem + S::kOffScr);
     float2 *sml = reinterpret_cast<float2 *>(smem + S::kOffML);
     uint32_t e = 0;
@@ -790,158 +978,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         named_barrier_sync(1, kConsumerWarps * 32);
         if (s_stop) return;
 
-        float o[D / 8][4];
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        if (have_q) {
-            const int kb0 = d.kb0, kb1 = d.kb1, kv_end = d.kv_end;
-            const int lim0 = d.row_limit[qrow], lim1 = d.row_limit[qrow + 8];
-
-            // Q fragments (A operand, 16 rows x D) for the whole item. Rows
-            // past n_valid hold stale data; they only affect their own rows,
-            // which are never written.
-            uint32_t qa[D / 16][4];
-            {
-                const uint32_t qs = smem_u32(smem + S::kOffQ + qb * S::kQBytes);
-                const int mi = lane >> 3;
-                const int row = ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int chunk = 2 * kk + (mi >> 1);
-                    ldmatrix_x4(qs + row * S::kQStride + chunk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-                }
-            }
-
-            for (int kb = kb0; kb < kb1; ++kb, ++e) {
-                if (((kb - kb0) & (kConsumerWarps - 1)) != warp) continue;
-                const int stage = e % S::kStages;
-                if (!mbar_wait(&full[stage], (e / S::kStages) & 1, status, abort)) break;
-                uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
-                const uint32_t kbase = smem_u32(st), vbase = kbase + S::kTileBytes;
-                const int key0 = kb * PKV_BLOCK_SIZE;
-
-                // Rows of V past the tile's last visible key may hold anything
-                // (other requests' stale data, NaN); their P is 0, but 0 * NaN
-                // is not, so clear them.
-                const bool tail = key0 + PKV_BLOCK_SIZE > kv_end;
-                if (tail) {
-                    const int first = kv_end - key0;  // 1..15
-                    for (int c = lane; c < (PKV_BLOCK_SIZE - first) * S::kBoxes * 8; c += 32) {
-                        const int row = first + c / (S::kBoxes * 8);
-                        const int rem = c % (S::kBoxes * 8);
-                        *reinterpret_cast<uint4 *>(st + S::kTileBytes + (rem >> 3) * 2048 + row * 128 +
-                                                   (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    __syncwarp();
-                }
-
-                // S = Q K^T for 16 keys: two n-tiles of 8 keys.
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                {
-                    const int mi = lane >> 3;
-                    const int key = ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const int chunk = 2 * kk + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                        mma_bf16_16816(sc[1], qa[kk], b2, b3);
-                    }
-                }
-
-                // Scale into the log2 domain, causal mask, online softmax.
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int key = key0 + nt * 8 + qcol + c;
-                        const float s0 = key <= lim0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
-                        const float s1 = key <= lim1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
-                        sc[nt][c] = s0;
-                        sc[nt][2 + c] = s1;
-                        mx0 = fmaxf(mx0, s0);
-                        mx1 = fmaxf(mx1, s1);
-                    }
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-                m0 = mn0;
-                m1 = mn1;
-                float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        sc[nt][c] = fast_exp2(sc[nt][c] - base0);
-                        sc[nt][2 + c] = fast_exp2(sc[nt][2 + c] - base1);
-                        ps0 += sc[nt][c];
-                        ps1 += sc[nt][2 + c];
-                    }
-                }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-                    for (int i = 0; i < D / 8; ++i) {
-                        o[i][0] *= al0; o[i][1] *= al0;
-                        o[i][2] *= al1; o[i][3] *= al1;
-                    }
-                }
-
-                // O += P V: P (16 rows x 16 keys) as the A operand.
-                uint32_t pa[4];
-                pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-                pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-                pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-                pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-                {
-                    const int mi = lane >> 3;
-                    const int key = ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int dp = 0; dp < D / 16; ++dp) {
-                        const int chunk = 2 * dp + (mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), b0, b1, b2, b3);
-                        mma_bf16_16816(o[2 * dp], pa, b0, b1);
-                        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    if (tail) fence_proxy_async_smem();
-                    mbar_arrive(&empty[stage]);
-                }
-            }
-        }
-
-        // Combine the four warps' states: each warp's rows -> scratch.
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        {
-            float *ws = scr + warp * kRowsPerTile * S::kScrStride;
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                const int col = i * 8 + qcol;
-                *reinterpret_cast<float2 *>(ws + qrow * S::kScrStride + col) = make_float2(o[i][0], o[i][1]);
-                *reinterpret_cast<float2 *>(ws + (qrow + 8) * S::kScrStride + col) = make_float2(o[i][2], o[i][3]);
-            }
-            if ((lane & 3) == 0) {
-                sml[warp * kRowsPerTile + qrow] = make_float2(m0, l0);
-                sml[warp * kRowsPerTile + qrow + 8] = make_float2(m1, l1);
-            }
-        }
+        if (d.n_valid <= 8)
+            consume_item<D, 1>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
+        else
+            consume_item<D, 2>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
         named_barrier_sync(1, kConsumerWarps * 32);
         const int n_valid = d.n_valid;
         const bool partial = d.partial != 0;
