@@ -704,10 +704,10 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
 //
 // The products run transposed, with the query rows as the mma's N = 8
 // dimension: S^T (16 keys x 8 rows) = K Q^T and O^T (D x 8 rows) += V^T P^T.
-// An item with at most 8 valid rows (a decode token's GQA group up to 8)
-// then costs half the mma instructions of a 16-row tile; the legacy mma
-// path sets this kernel's per-block rate, which with 16-row products is
-// about the HBM rate itself. P^T goes from the accumulator layout to the B
+// One 8-row n-tile (NT = 1) costs half the mma instructions of a 16-row
+// tile, most of whose rows are padding for a decode token's GQA group of 4;
+// with 16-row products the legacy mma path sets a per-block rate about equal
+// to the HBM rate itself. P^T goes from the accumulator layout to the B
 // operand layout with two 8x8 register transposes (movmatrix).
 template <int D, int NT>
 __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem, const ItemDesc &d, int qb,
@@ -888,6 +888,171 @@ __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem,
     }
 }
 
+// One consumer warp's share of an item with more than 4 valid rows: its
+// blocks against all 16 rows of the tile (S = Q K^T, O += P V with the rows
+// as M = 16), then its unnormalised O, running max and sum per row into the
+// CTA's scratch.
+template <int D>
+__device__ __forceinline__ void consume_item16(const DecodeArgs &a, uint8_t *smem, const ItemDesc &d, int qb,
+                                               uint64_t *full, uint64_t *empty, uint32_t &e, int32_t *status,
+                                               volatile int *abort, int warp, int lane, float *scr, float2 *sml) {
+    using S = DecodeSmem<D>;
+    const int qrow = lane >> 2;  // fragment rows qrow and qrow + 8
+    const int qcol = (lane & 3) * 2;
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    {
+        const int kb0 = d.kb0, kb1 = d.kb1, kv_end = d.kv_end;
+        const int lim0 = d.row_limit[qrow], lim1 = d.row_limit[qrow + 8];
+
+        // Q fragments (A operand, 16 rows x D) for the whole item. Rows
+        // past n_valid hold stale data; they only affect their own rows,
+        // which are never written.
+        uint32_t qa[D / 16][4];
+        {
+            const uint32_t qs = smem_u32(smem + S::kOffQ + qb * S::kQBytes);
+            const int mi = lane >> 3;
+            const int row = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int chunk = 2 * kk + (mi >> 1);
+                ldmatrix_x4(qs + row * S::kQStride + chunk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            }
+        }
+
+        for (int kb = kb0; kb < kb1; ++kb, ++e) {
+            if (((kb - kb0) & (kConsumerWarps - 1)) != warp) continue;
+            const int stage = e % S::kStages;
+            if (!mbar_wait(&full[stage], (e / S::kStages) & 1, status, abort)) break;
+            uint8_t *st = smem + S::kOffStages + stage * S::kStageBytes;
+            const uint32_t kbase = smem_u32(st), vbase = kbase + S::kTileBytes;
+            const int key0 = kb * PKV_BLOCK_SIZE;
+
+            // Rows of V past the tile's last visible key may hold anything
+            // (other requests' stale data, NaN); their P is 0, but 0 * NaN
+            // is not, so clear them.
+            const bool tail = key0 + PKV_BLOCK_SIZE > kv_end;
+            if (tail) {
+                const int first = kv_end - key0;  // 1..15
+                for (int c = lane; c < (PKV_BLOCK_SIZE - first) * S::kBoxes * 8; c += 32) {
+                    const int row = first + c / (S::kBoxes * 8);
+                    const int rem = c % (S::kBoxes * 8);
+                    *reinterpret_cast<uint4 *>(st + S::kTileBytes + (rem >> 3) * 2048 + row * 128 +
+                                               (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // S = Q K^T for 16 keys: two n-tiles of 8 keys.
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3;
+                const int key = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int chunk = 2 * kk + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(kbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                }
+            }
+
+            // Scale into the log2 domain, causal mask, online softmax.
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int key = key0 + nt * 8 + qcol + c;
+                    const float s0 = key <= lim0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
+                    const float s1 = key <= lim1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+                    sc[nt][c] = s0;
+                    sc[nt][2 + c] = s1;
+                    mx0 = fmaxf(mx0, s0);
+                    mx1 = fmaxf(mx1, s1);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    sc[nt][c] = fast_exp2(sc[nt][c] - base0);
+                    sc[nt][2 + c] = fast_exp2(sc[nt][2 + c] - base1);
+                    ps0 += sc[nt][c];
+                    ps1 += sc[nt][2 + c];
+                }
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) {
+                    o[i][0] *= al0; o[i][1] *= al0;
+                    o[i][2] *= al1; o[i][3] *= al1;
+                }
+            }
+
+            // O += P V: P (16 rows x 16 keys) as the A operand.
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+            pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+            pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+            pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+            {
+                const int mi = lane >> 3;
+                const int key = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int dp = 0; dp < D / 16; ++dp) {
+                    const int chunk = 2 * dp + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(vbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * dp], pa, b0, b1);
+                    mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (tail) fence_proxy_async_smem();
+                mbar_arrive(&empty[stage]);
+            }
+        }
+    }
+
+    // Combine the four warps' states: each warp's rows -> scratch.
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    {
+        float *ws = scr + warp * kRowsPerTile * S::kScrStride;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            const int col = i * 8 + qcol;
+            *reinterpret_cast<float2 *>(ws + qrow * S::kScrStride + col) = make_float2(o[i][0], o[i][1]);
+            *reinterpret_cast<float2 *>(ws + (qrow + 8) * S::kScrStride + col) = make_float2(o[i][2], o[i][3]);
+        }
+        if ((lane & 3) == 0) {
+            sml[warp * kRowsPerTile + qrow] = make_float2(m0, l0);
+            sml[warp * kRowsPerTile + qrow + 8] = make_float2(m1, l1);
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, D == 128 ? 2 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
@@ -978,10 +1143,13 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         named_barrier_sync(1, kConsumerWarps * 32);
         if (s_stop) return;
 
-        if (d.n_valid <= 8)
+        // Up to 4 rows (a decode token's GQA group of 4 or fewer): the
+        // transposed 8-row products; more: 16-row products, whose shorter
+        // per-block dependency chain matters more than their padding.
+        if (d.n_valid <= 4)
             consume_item<D, 1>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
         else
-            consume_item<D, 2>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
+            consume_item16<D>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
         named_barrier_sync(1, kConsumerWarps * 32);
         const int n_valid = d.n_valid;
         const bool partial = d.partial != 0;
