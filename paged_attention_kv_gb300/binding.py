@@ -340,6 +340,13 @@ class StepBuffers:
         self.out = torch.empty_like(self.q)
         self.workspace = alloc_workspace(batch.num_reqs, self.num_tokens, batch.shape.num_q_heads, self.kv_cache)
 
+    def prepared(self, stream=None) -> "PreparedStep":
+        """This step's three calls with their C arguments built once (for
+        loops that enqueue the same step many times: the per-call checks and
+        argument conversion of the wrappers cost the host more than a small
+        step costs the GPU). Valid while these buffers stay in place."""
+        return PreparedStep(self, stream)
+
     def step(self, stream=None):
         """Slot mapping, KV write and attention, enqueued on `stream`."""
         paged_slot_mapping(self.block_table, self.seq_lens, self.query_start_loc, self.num_tokens,
@@ -348,6 +355,53 @@ class StepBuffers:
         paged_attention(self.q, self.kv_cache, self.block_table, self.seq_lens, self.query_start_loc,
                         self.batch.scale, self.out, self.workspace, stream, max_query_len=self.max_query_len)
         return self.out
+
+
+class PreparedStep:
+    """Slot mapping, KV write and attention of a StepBuffers, checked once,
+    then enqueued by calling the object: three C calls with prebuilt
+    arguments and no per-call Python checks."""
+
+    def __init__(self, buf: "StepBuffers", stream=None):
+        for t, dt, nd, name in ((buf.q, torch.bfloat16, 3, "q"), (buf.k, torch.bfloat16, 3, "k"),
+                                (buf.v, torch.bfloat16, 3, "v"), (buf.kv_cache, torch.bfloat16, 5, "kv_cache"),
+                                (buf.block_table, torch.int32, 2, "block_table"),
+                                (buf.seq_lens, torch.int32, 1, "seq_lens"),
+                                (buf.query_start_loc, torch.int32, 1, "query_start_loc"),
+                                (buf.slot_mapping, torch.int32, 1, "slot_mapping"),
+                                (buf.status, torch.int32, 1, "status"), (buf.out, torch.bfloat16, 3, "out")):
+            _want(t, dt, nd, name)
+        if not buf.workspace.is_cuda or not buf.workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        b = buf.batch
+        self.desc = cache_desc(buf.kv_cache)  # kept alive: passed by reference
+        t, hq, _ = buf.q.shape
+        r = b.num_reqs
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        st = _stream(stream)
+        desc = ctypes.byref(self.desc)
+        ws_bytes = ctypes.c_size_t(buf.workspace.numel() * buf.workspace.element_size())
+        self.calls = (
+            ("paged_slot_mapping", LIB.paged_slot_mapping,
+             (_ptr(buf.block_table), i32(r), i32(buf.block_table.shape[1]), _ptr(buf.seq_lens),
+              _ptr(buf.query_start_loc), i32(buf.num_tokens), i32(b.num_blocks), _ptr(buf.slot_mapping),
+              _ptr(buf.status), st)),
+            ("paged_kv_write", LIB.paged_kv_write,
+             (_ptr(buf.k), _ptr(buf.v), _ptr(buf.slot_mapping), i32(buf.k.shape[0]), _ptr(buf.kv_cache), desc,
+              _ptr(buf.status), st)),
+            ("paged_attention_bounded", LIB.paged_attention_bounded,
+             (_ptr(buf.q), i32(t), i32(hq), _ptr(buf.kv_cache), desc, _ptr(buf.block_table), i32(r),
+              i32(buf.block_table.shape[1]), _ptr(buf.seq_lens), _ptr(buf.query_start_loc),
+              i32(buf.max_query_len), ctypes.c_float(b.scale), _ptr(buf.out), _ptr(buf.workspace), ws_bytes, st,
+              None)),
+        )
+        self.buf = buf  # keeps the tensors alive
+
+    def __call__(self) -> None:
+        for name, fn, args in self.calls:
+            rc = fn(*args)
+            if rc != PKV_OK:
+                raise PagedKVError(rc, name)
 
 
 class StepGraph:

@@ -401,6 +401,25 @@ def test_max_query_len_bound_skips_the_chunk_kernel_and_stays_correct():
     assert_attention_close(buf.out, ref, what="too-small bound")
 
 
+@pytest.mark.parametrize("workload", ["tiny", "mixed"])
+def test_prepared_step_matches_the_checked_calls(workload):
+    """StepBuffers.prepared(): the same three C calls with prebuilt
+    arguments give the same slot mapping, pool and output bits."""
+    batch = wl.make_batch(workload)
+    ten = device_tensors(batch, generate_on="cpu")
+    a = pkv.StepBuffers(batch, {k: v.clone() for k, v in ten.items()})
+    b = pkv.StepBuffers(batch, {k: v.clone() for k, v in ten.items()})
+    a.step()
+    run = b.prepared()
+    run()
+    torch.cuda.synchronize()
+    for buf in (a, b):
+        assert pkv.pkv_read_status(buf.status) == 0 and pkv.pkv_read_status(buf.workspace) == 0
+    assert torch.equal(a.slot_mapping, b.slot_mapping)
+    assert torch.equal(a.kv_cache.view(torch.int16), b.kv_cache.view(torch.int16))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
 def test_a_wait_that_never_completes_is_reported_and_the_context_survives():
     """Failure detection without a fault: the self-test's wait on a barrier
     that nothing arrives on gives up after 2 ms, the status word carries
