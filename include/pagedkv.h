@@ -277,6 +277,70 @@ int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_head
                            float scale, void *out, void *stream);
 
 /*
+ * Host-buffer step pipeline: steps whose inputs come from, and whose output
+ * goes to, pinned host memory, with the copies overlapped across steps
+ * (the engine loop's per-step transfer of the batch's tensors and metadata,
+ * "Run forward pass"). The caller owns every buffer; the pipeline owns only
+ * CUDA events. Each step:
+ *   h2d stream:     one copy of slot s's packed inputs (host_in[s] ->
+ *                   dev_in[s]), after the step that last used slot s has
+ *                   finished its kernels;
+ *   compute stream: paged_slot_mapping, paged_kv_write and
+ *                   paged_attention_bounded on slot s's device arrays,
+ *                   after that copy and after slot s's previous output has
+ *                   left the device;
+ *   d2h stream:     one copy of slot s's output to the caller's host
+ *                   buffer.
+ * Slots are used in turn (step i uses slot i % depth). Packed inputs of a
+ * slot: q [num_tokens][num_q_heads][head_size] bf16, k and v
+ * [num_tokens][num_kv_heads][head_size] bf16, block_table
+ * [max_num_reqs][max_blocks_per_req] int32, seq_lens [max_num_reqs] int32,
+ * query_start_loc [max_num_reqs + 1] int32, at the given byte offsets.
+ */
+#define PKV_PIPELINE_MAX_DEPTH 4
+typedef struct {
+    int32_t depth;                     /* slots, 1 .. PKV_PIPELINE_MAX_DEPTH */
+    void *host_in[PKV_PIPELINE_MAX_DEPTH];  /* pinned host packed inputs, in_bytes each */
+    void *dev_in[PKV_PIPELINE_MAX_DEPTH];   /* device packed inputs, same layout */
+    size_t in_bytes;
+    size_t off_q, off_k, off_v, off_block_table, off_seq_lens, off_query_start_loc;  /* 16-byte aligned */
+    int32_t num_tokens, num_q_heads, max_num_reqs, max_blocks_per_req;
+    pkv_cache_desc cache;              /* every pool the steps use has this shape */
+    int32_t *slot_mapping[PKV_PIPELINE_MAX_DEPTH];  /* device int32 [num_tokens] */
+    void *out[PKV_PIPELINE_MAX_DEPTH];              /* device bf16 [num_tokens][num_q_heads][head_size] */
+    int32_t *status;                   /* device status word of slot mapping and KV write */
+    void *workspace;                   /* attention workspace, workspace_bytes */
+    size_t workspace_bytes;
+    float scale;
+    void *h2d_stream, *compute_stream, *d2h_stream;  /* cudaStream_t (NULL: the legacy default stream);
+                                                        distinct streams overlap the copies with the
+                                                        neighbouring steps' kernels, equal ones serialise */
+} pkv_pipeline_desc;
+typedef struct pkv_pipeline pkv_pipeline;
+
+/* Checks the description and creates the pipeline's events. The pointers
+ * in `desc` must stay valid until pkv_pipeline_destroy. */
+int pkv_pipeline_create(const pkv_pipeline_desc *desc, pkv_pipeline **pipeline);
+
+/* The slot the next submit uses; waits (host) until that slot's previous
+ * input copy has been read, so its host_in may be rewritten. */
+int pkv_pipeline_next(pkv_pipeline *pipeline, int32_t *slot);
+
+/* Enqueues the next step: num_reqs requests (1 .. max_num_reqs) of the
+ * slot's inputs against kv_cache (a pool of desc.cache's shape), output to
+ * out_host (pinned, num_tokens * num_q_heads * head_size bf16).
+ * max_query_len as for paged_attention_bounded; a negative value takes it
+ * from the slot's host query_start_loc. Does not wait. */
+int pkv_pipeline_submit(pkv_pipeline *pipeline, int32_t num_reqs, void *kv_cache, void *out_host,
+                        int32_t max_query_len);
+
+/* Waits until every submitted step's output is in host memory. */
+int pkv_pipeline_sync(pkv_pipeline *pipeline);
+
+/* Waits for the submitted steps, then frees the pipeline's events. */
+int pkv_pipeline_destroy(pkv_pipeline *pipeline);
+
+/*
  * Failure-detection self-test: runs one thread that waits, with the bounded
  * wait every pipeline stage of the attention kernels uses, on an mbarrier
  * that nothing arrives on. After timeout_us (1 .. 1000000) the wait gives

@@ -40,7 +40,8 @@ PKV_DEV_OVERFLOW = 0x20
 EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_gather_blocks",
             "paged_kv_scatter_blocks", "paged_attention_workspace_bytes",
             "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
-            "paged_attention_bounded", "paged_attention_static", "pkv_read_status", "pkv_selftest_bounded_wait", "pkv_status_string")
+            "paged_attention_bounded", "paged_attention_static", "pkv_pipeline_create", "pkv_pipeline_next",
+            "pkv_pipeline_submit", "pkv_pipeline_sync", "pkv_pipeline_destroy", "pkv_read_status", "pkv_selftest_bounded_wait", "pkv_status_string")
 
 
 class PagedKVError(RuntimeError):
@@ -52,6 +53,24 @@ class PagedKVError(RuntimeError):
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_size", ctypes.c_int32)]
+
+
+PIPELINE_MAX_DEPTH = 4
+
+
+class PipelineDesc(ctypes.Structure):
+    """pkv_pipeline_desc of include/pagedkv.h."""
+    _fields_ = [("depth", ctypes.c_int32), ("host_in", ctypes.c_void_p * PIPELINE_MAX_DEPTH),
+                ("dev_in", ctypes.c_void_p * PIPELINE_MAX_DEPTH), ("in_bytes", ctypes.c_size_t),
+                ("off_q", ctypes.c_size_t), ("off_k", ctypes.c_size_t), ("off_v", ctypes.c_size_t),
+                ("off_block_table", ctypes.c_size_t), ("off_seq_lens", ctypes.c_size_t),
+                ("off_query_start_loc", ctypes.c_size_t), ("num_tokens", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("max_num_reqs", ctypes.c_int32),
+                ("max_blocks_per_req", ctypes.c_int32), ("cache", CacheDesc),
+                ("slot_mapping", ctypes.c_void_p * PIPELINE_MAX_DEPTH), ("out", ctypes.c_void_p * PIPELINE_MAX_DEPTH),
+                ("status", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("scale", ctypes.c_float), ("h2d_stream", ctypes.c_void_p), ("compute_stream", ctypes.c_void_p),
+                ("d2h_stream", ctypes.c_void_p)]
 
 
 def _load():
@@ -73,6 +92,11 @@ def _load():
                                             vp, sz, vp, ctypes.POINTER(vp)]
     lib.paged_attention_static.argtypes = [vp, i32, i32, vp, desc_p, vp, i32, i32, vp, vp, ctypes.c_float, vp, vp]
     lib.pkv_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
+    lib.pkv_pipeline_create.argtypes = [ctypes.POINTER(PipelineDesc), ctypes.POINTER(vp)]
+    lib.pkv_pipeline_next.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.pkv_pipeline_submit.argtypes = [vp, i32, vp, vp, i32]
+    lib.pkv_pipeline_sync.argtypes = [vp]
+    lib.pkv_pipeline_destroy.argtypes = [vp]
     lib.pkv_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -438,8 +462,10 @@ class HostStepPipeline:
     step i computes, and step i's output returns on a second copy stream
     while step i+1 computes. Each step is the same three calls as
     ``StepBuffers.step`` (slot mapping, KV write, attention) on the compute
-    stream, so steps still run in order against the pool. Only the copies,
-    streams and events are PyTorch's.
+    stream, so steps still run in order against the pool. The copies, the
+    calls and the events that order them are the library's native pipeline
+    (``pkv_pipeline_*``, one C call per step); the buffers and streams are
+    PyTorch's.
 
     Use: ``inp = pipe.next_inputs()`` (host views q, k, v, block_table,
     seq_lens, query_start_loc of the next slot; waits until that slot's
@@ -492,13 +518,41 @@ class HostStepPipeline:
         self.dev_in = [views(r) for r in self.dev_raw]
         self.slot_mapping = [torch.empty(T, dtype=torch.int32, device=dev) for _ in range(self.depth)]
         self.out = [torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) for _ in range(self.depth)]
-        self.loaded = [torch.cuda.Event() for _ in range(self.depth)]
-        self.computed = [torch.cuda.Event() for _ in range(self.depth)]
-        self.returned = [torch.cuda.Event() for _ in range(self.depth)]
-        self.used = [False] * self.depth
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspace = alloc_workspace(R, self.num_tokens, Hq, kv_cache)
+        if not 1 <= self.depth <= PIPELINE_MAX_DEPTH:
+            raise PagedKVError(PKV_E_DIMS, "pipeline depth outside 1..4")
+        desc = PipelineDesc()
+        desc.depth = self.depth
+        for i in range(self.depth):
+            desc.host_in[i] = self.host_raw[i].data_ptr()
+            desc.dev_in[i] = self.dev_raw[i].data_ptr()
+            desc.slot_mapping[i] = self.slot_mapping[i].data_ptr()
+            desc.out[i] = self.out[i].data_ptr()
+        desc.in_bytes = off
+        desc.off_q, desc.off_k, desc.off_v, desc.off_block_table, desc.off_seq_lens, desc.off_query_start_loc = offs
+        desc.num_tokens, desc.num_q_heads, desc.max_num_reqs, desc.max_blocks_per_req = T, Hq, R, M
+        desc.cache = d
+        desc.status = self.status.data_ptr()
+        desc.workspace = self.workspace.data_ptr()
+        desc.workspace_bytes = self.workspace.numel() * self.workspace.element_size()
+        desc.scale = self.scale
+        desc.h2d_stream = self.h2d.cuda_stream
+        desc.compute_stream = self.compute.cuda_stream
+        desc.d2h_stream = self.d2h.cuda_stream
+        self._desc = desc
+        handle = ctypes.c_void_p(0)
+        _check(LIB.pkv_pipeline_create(ctypes.byref(desc), ctypes.byref(handle)), "pkv_pipeline_create")
+        self._handle = handle
+        self._lib = LIB
+        self._slot = ctypes.c_int32(0)
         self.i = 0
+
+    def __del__(self):
+        handle = getattr(self, "_handle", None)
+        if handle is not None and handle.value:
+            self._lib.pkv_pipeline_destroy(handle)
+            self._handle = None
 
     def slot_inputs(self, slot: int) -> dict:
         """Host views of one slot, for filling every slot before the first
@@ -506,58 +560,35 @@ class HostStepPipeline:
         return self.host_in[slot]
 
     def next_inputs(self) -> dict:
-        """Host views to fill with the next step's inputs."""
-        b = self.i % self.depth
-        if self.used[b]:
-            self.loaded[b].synchronize()  # the slot's previous copy has been read
-        return self.host_in[b]
+        """Host views to fill with the next step's inputs (waits until that
+        slot's previous input copy has been read)."""
+        _check(LIB.pkv_pipeline_next(self._handle, ctypes.byref(self._slot)), "pkv_pipeline_next")
+        return self.host_in[self._slot.value]
 
     def submit(self, out_host: torch.Tensor, num_reqs: int | None = None, kv_cache=None,
-               max_query_len: int | None = None) -> torch.cuda.Event:
-        """Enqueue the step whose inputs are in ``next_inputs()``; returns the
-        event after which ``out_host`` holds its output. ``num_reqs``: the
-        requests of this step (default: all). ``kv_cache``: this step's pool
-        when it is not the one the pipeline was built with (another layer's
-        pool of the same shape). ``max_query_len``: the longest request of
-        the step, as the scheduler knows it (default: taken from the host
-        copy of query_start_loc; 0: unknown)."""
+               max_query_len: int | None = None) -> None:
+        """Enqueue the step whose inputs are in ``next_inputs()`` (one C call:
+        the input copy, the three calls and the output copy, ordered by the
+        pipeline's events). ``num_reqs``: the requests of this step (default:
+        all). ``kv_cache``: this step's pool when it is not the one the
+        pipeline was built with (another layer's pool of the same shape).
+        ``max_query_len``: the longest request of the step, as the scheduler
+        knows it (default: taken from the host copy of query_start_loc).
+        ``out_host`` (pinned, the output's shape) holds the output after
+        ``synchronize()``."""
         pool = self.kv_cache if kv_cache is None else kv_cache
         if pool.shape != self.kv_cache.shape or pool.dtype != self.kv_cache.dtype:
             raise PagedKVError(PKV_E_DIMS, "kv_cache differs in shape from the pipeline's pool")
+        if out_host.numel() * out_host.element_size() != self.out[0].numel() * self.out[0].element_size():
+            raise PagedKVError(PKV_E_DIMS, "out_host differs in size from the step's output")
         R = self.max_num_reqs if num_reqs is None else int(num_reqs)
-        if not 0 < R <= self.max_num_reqs:
-            raise PagedKVError(PKV_E_DIMS, "num_reqs outside the pipeline's bounds")
-        b = self.i % self.depth
-        din = self.dev_in[b]
-        if max_query_len is None:
-            hq = self.host_in[b]["query_start_loc"][:R + 1]
-            max_query_len = int((hq[1:] - hq[:-1]).max())
-        with torch.cuda.stream(self.h2d):
-            if self.used[b]:
-                self.h2d.wait_event(self.computed[b])  # the step that last read this slot is done
-            self.dev_raw[b].copy_(self.host_raw[b], non_blocking=True)
-            self.loaded[b].record(self.h2d)
-        self.compute.wait_event(self.loaded[b])
-        if self.used[b]:
-            self.compute.wait_event(self.returned[b])  # its previous output has left the device
-        bt, sl, qsl = din["block_table"][:R], din["seq_lens"][:R], din["query_start_loc"][:R + 1]
-        paged_slot_mapping(bt, sl, qsl, self.num_tokens, self.num_blocks, self.slot_mapping[b], self.status,
-                           self.compute)
-        paged_kv_write(din["k"], din["v"], self.slot_mapping[b], pool, self.status, self.compute)
-        paged_attention(din["q"], pool, bt, sl, qsl, self.scale, self.out[b], self.workspace, self.compute,
-                        max_query_len=max(0, max_query_len))
-        self.computed[b].record(self.compute)
-        with torch.cuda.stream(self.d2h):
-            self.d2h.wait_event(self.computed[b])
-            out_host.copy_(self.out[b], non_blocking=True)
-            self.returned[b].record(self.d2h)
-        self.used[b] = True
+        mq = -1 if max_query_len is None else max(0, int(max_query_len))
+        _check(LIB.pkv_pipeline_submit(self._handle, R, pool.data_ptr(), out_host.data_ptr(), mq),
+               "pkv_pipeline_submit")
         self.i += 1
-        return self.returned[b]
 
     def synchronize(self) -> None:
-        for st in (self.h2d, self.compute, self.d2h):
-            st.synchronize()
+        _check(LIB.pkv_pipeline_sync(self._handle), "pkv_pipeline_sync")
 
     def read_status(self) -> tuple[int, int]:
         """(slot mapping / KV write status, attention status)."""

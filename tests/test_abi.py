@@ -110,3 +110,49 @@ def test_min_workspace_is_host_only_and_below_default_layout():
     assert out.value > 0
     # A workspace one byte short is rejected before any CUDA call.
     assert _attn(d, t=256, r=256, wsb=out.value - 1) == pkv.PKV_E_WORKSPACE
+
+
+def _pipeline_desc(**kw):
+    d = pkv.PipelineDesc()
+    d.depth = 2
+    for i in range(2):
+        d.host_in[i], d.dev_in[i] = 0x100000 * (i + 1), 0x200000 * (i + 1)
+        d.slot_mapping[i], d.out[i] = 0x300000 + 0x1000 * i, 0x400000 + 0x10000 * i
+    T, hq, hkv, D, R, M = 4, 32, 8, 128, 4, 8
+    d.off_q, d.off_k, d.off_v = 0, T * hq * D * 2, T * hq * D * 2 + T * hkv * D * 2
+    d.off_block_table = d.off_v + T * hkv * D * 2
+    d.off_seq_lens = d.off_block_table + R * M * 4
+    d.off_query_start_loc = d.off_seq_lens + 256
+    d.in_bytes = d.off_query_start_loc + 256
+    d.num_tokens, d.num_q_heads, d.max_num_reqs, d.max_blocks_per_req = T, hq, R, M
+    d.cache = _desc(nb=64, hkv=hkv, d=D)
+    d.status, d.workspace, d.workspace_bytes, d.scale = 0x500000, 0x600000, 1 << 20, 0.088
+    d.h2d_stream, d.compute_stream, d.d2h_stream = 0x11, 0x22, 0x33
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_pipeline_create_validates_the_description_before_any_cuda_call():
+    h = ctypes.c_void_p(0)
+    create = pkv.LIB.pkv_pipeline_create
+    assert create(None, ctypes.byref(h)) == pkv.PKV_E_NULL
+    assert create(ctypes.byref(_pipeline_desc(depth=0)), ctypes.byref(h)) == pkv.PKV_E_DIMS
+    assert create(ctypes.byref(_pipeline_desc(depth=5)), ctypes.byref(h)) == pkv.PKV_E_DIMS
+    assert create(ctypes.byref(_pipeline_desc(num_q_heads=12)), ctypes.byref(h)) == pkv.PKV_E_GQA
+    assert create(ctypes.byref(_pipeline_desc(status=None)), ctypes.byref(h)) == pkv.PKV_E_NULL
+    bad = _pipeline_desc()
+    bad.in_bytes = bad.off_query_start_loc + 8          # query_start_loc does not fit
+    assert create(ctypes.byref(bad), ctypes.byref(h)) == pkv.PKV_E_DIMS
+    bad = _pipeline_desc()
+    bad.off_k += 8                                      # k not 16-byte aligned
+    assert create(ctypes.byref(bad), ctypes.byref(h)) == pkv.PKV_E_DIMS
+    bad = _pipeline_desc()
+    bad.cache = _desc(nb=64, hkv=8, d=96)               # attention head size
+    assert create(ctypes.byref(bad), ctypes.byref(h)) == pkv.PKV_E_HEAD_SIZE
+    assert h.value is None
+    slot = ctypes.c_int32(0)
+    assert pkv.LIB.pkv_pipeline_next(None, ctypes.byref(slot)) == pkv.PKV_E_NULL
+    assert pkv.LIB.pkv_pipeline_submit(None, 1, None, None, -1) == pkv.PKV_E_NULL
+    assert pkv.LIB.pkv_pipeline_sync(None) == pkv.PKV_E_NULL
+    assert pkv.LIB.pkv_pipeline_destroy(None) == pkv.PKV_OK
