@@ -66,8 +66,10 @@ def parse_args():
                         "per model layer, as a real step over a model's layers does) until their total exceeds "
                         "512 MiB; flush: write and read 512 MiB before every step and time steps one by one; "
                         "auto: layers when one pool is under 512 MiB, else none (the step's reads are GBs)")
-    p.add_argument("--op", choices=("step", "kv_transfer"), default="step",
-                   help="kv_transfer: time block gather + scatter of the workload's context blocks")
+    p.add_argument("--op", choices=("step", "kv_transfer", "kv_write"), default="step",
+                   help="kv_transfer: time block gather + scatter of the workload's context blocks; "
+                        "kv_write: time the KV write alone, on the workload's new tokens and on a "
+                        "prefill-sized token count")
     return p.parse_args()
 
 
@@ -419,6 +421,9 @@ def main():
     if args.op == "kv_transfer":
         run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world)
         return
+    if args.op == "kv_write":
+        run_kv_write(args, batch, ten, pkv, torch, dev, dist, rank, world)
+        return
     host = host_copy(ten) if (rank == 0 and world == 1 and not args.skip_cpu_baseline) else None
     mode, layers = l2_mode(args, batch)
     bufs = [pkv.StepBuffers(batch, ten)]
@@ -597,6 +602,78 @@ def run_kv_transfer(args, batch, ten, pkv, torch, dev, dist, rank, world):
                                         "bytes_per_step": nbytes},
         "roofline": {"bound": "hbm", "kernel": "block_copy_kernel", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps}), flush=True)
+
+
+KV_WRITE_BIG_TOKENS = 65536
+
+
+def run_kv_write(args, batch, ten, pkv, torch, dev, dist, rank, world):
+    """The KV write alone (the scatter of this step's K/V into the pool
+    through the slot mapping). Bytes per call: K and V read (2 T Hkv D 2),
+    the same written, and the slot mapping (4 T). Timed on the workload's
+    own new tokens (small: L2-resident, launch-bound) and on a prefill-sized
+    count, KV_WRITE_BIG_TOKENS tokens into distinct slots of a pool of
+    1.25x the blocks they need (seeded permutation), which is HBM-bound."""
+    s = batch.shape
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    slots = pkv.paged_slot_mapping(torch.from_numpy(batch.block_table).to(dev),
+                                   torch.from_numpy(batch.seq_lens).to(dev),
+                                   torch.from_numpy(batch.query_start_loc).to(dev), batch.num_tokens,
+                                   batch.num_blocks, status=status)
+    T = KV_WRITE_BIG_TOKENS
+    nblk = -(-T // 16)
+    pool_blocks = nblk * 5 // 4
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(batch.seed + 7)
+    k_big = torch.randn((T, s.num_kv_heads, s.head_size), device=dev, generator=gen).to(torch.bfloat16)
+    v_big = torch.randn((T, s.num_kv_heads, s.head_size), device=dev, generator=gen).to(torch.bfloat16)
+    pool_big = torch.zeros((pool_blocks, 2, s.num_kv_heads, 16, s.head_size), dtype=torch.bfloat16, device=dev)
+    perm = torch.randperm(pool_blocks, device=dev, generator=gen)[:nblk].to(torch.int32)
+    tok = torch.arange(T, device=dev, dtype=torch.int32)
+    slots_big = (perm[tok // 16] * 16 + tok % 16).to(torch.int32)
+    cases = {"step": (ten["k"], ten["v"], slots, ten["kv_cache"]), "prefill": (k_big, v_big, slots_big, pool_big)}
+    out = {}
+    import ctypes
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for name, (k, v, sl, pool) in cases.items():
+        pkv.paged_kv_write(k, v, sl, pool, status)  # the checked call once; the timed loop calls the C ABI directly
+        desc = pkv.cache_desc(pool)
+        cargs = (ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(sl.data_ptr()),
+                 ctypes.c_int32(k.shape[0]), ctypes.c_void_p(pool.data_ptr()), ctypes.byref(desc),
+                 ctypes.c_void_p(status.data_ptr()), stream)
+        for _ in range(max(3, args.warmup)):
+            pkv.LIB.paged_kv_write(*cargs)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            if pkv.LIB.paged_kv_write(*cargs) != 0:
+                raise RuntimeError("paged_kv_write failed")
+        b.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b), dist, dev) / args.steps
+        t = k.shape[0]
+        nbytes = 2 * 2 * t * s.num_kv_heads * s.head_size * 2 + 4 * t
+        out[name] = {"tokens": int(t), "bytes": nbytes, "us": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    if pkv.pkv_read_status(status):
+        raise RuntimeError("device status bits set")
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    big = out["prefill"]
+    print(json.dumps({
+        "metric": "KV write GB/s", "value": world * big["gbs"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": big["us"] / 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)", "data": "synthetic",
+        "config": {**workload_config(batch), "cases": out,
+                   "note": "value: the prefill-sized case; the step case is the workload's own new tokens "
+                           "(L2-resident, launch-bound)"},
+        "roofline": {"bound": "hbm", "kernel": "kv_write_kernel", "achieved": big["gbs"],
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": big["gbs"] / peaks["hbm_gbs"],
                      "traffic": None},
         "gpu_launches": 2 * args.steps}), flush=True)
 

@@ -54,36 +54,66 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int
     slot_mapping[t] = slot;
 }
 
-// One thread per 16-byte chunk of a (token, K|V, kv head) row; consecutive
-// threads walk a row, so reads of k/v and writes of each 16-row block tile
-// are contiguous.
+// Each warp takes R adjacent (token, K or V) rows per pass: a row (the
+// token's K or V for all kv heads) is contiguous in k / v, and each head's D
+// columns go to one row of a 16-row block tile. Slots and destinations are
+// worked out once per row; each lane then has R x (4 / R) = 4 16-byte loads
+// in flight before its stores (R = 1 for rows of >= 128 chunks, 4 for rows
+// of 32 or fewer).
+template <int R>
 __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                 const int32_t *__restrict__ slot_mapping, long long num_tokens,
                                 uint4 *__restrict__ kv_cache, long long num_slots, int num_kv_heads,
                                 int chunks_per_row, int32_t *status) {
     pdl_launch_dependents();
     pdl_wait();
-    const long long per_kv = (long long)num_kv_heads * chunks_per_row;
-    const long long total = num_tokens * 2 * per_kv;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long t = idx / (2 * per_kv);
-        const long long rem = idx - t * 2 * per_kv;
-        const int kv = (int)(rem / per_kv);
-        const long long hc = rem - kv * per_kv;   // h * chunks_per_row + c
-        const int32_t slot = __ldg(slot_mapping + t);
-        if (slot < 0) continue;
-        if ((long long)slot >= num_slots) {
-            if (rem == 0) raise_status(status, PKV_DEV_BAD_SLOT);
-            continue;
+    constexpr int C = 4 / R;  // chunks per lane per row and pass
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int per_kv = num_kv_heads * chunks_per_row;  // 16-byte chunks of one token's K (or V) row
+    const long long tile = (long long)PKV_BLOCK_SIZE * chunks_per_row;  // chunks of one (block, K|V, head) tile
+    const long long units = 2 * num_tokens;
+    for (long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g * R < units; g += nwarps) {
+        const uint4 *src[R];
+        uint4 *dst[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const long long u = g * R + j;
+            src[j] = nullptr;
+            dst[j] = nullptr;
+            if (u >= units) continue;
+            const long long t = u >> 1;
+            const int kv = (int)(u & 1);
+            const int32_t slot = __ldg(slot_mapping + t);
+            if (slot < 0) continue;
+            if ((long long)slot >= num_slots) {
+                if (lane == 0 && kv == 0) raise_status(status, PKV_DEV_BAD_SLOT);
+                continue;
+            }
+            src[j] = (kv ? v : k) + t * per_kv;
+            dst[j] = kv_cache + ((long long)slot / PKV_BLOCK_SIZE * 2 + kv) * num_kv_heads * tile +
+                     (long long)(slot % PKV_BLOCK_SIZE) * chunks_per_row;
         }
-        const int h = (int)(hc / chunks_per_row);
-        const int c = (int)(hc - (long long)h * chunks_per_row);
-        const uint4 val = __ldg((kv ? v : k) + t * per_kv + hc);
-        const long long block = slot / PKV_BLOCK_SIZE;
-        const int row = slot % PKV_BLOCK_SIZE;
-        const long long dst = (((block * 2 + kv) * num_kv_heads + h) * PKV_BLOCK_SIZE + row) * chunks_per_row + c;
-        kv_cache[dst] = val;
+        for (int base = 0; base < per_kv; base += 32 * C) {
+            uint4 val[R][C];
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    const int hc = base + c * 32 + lane;
+                    if (src[j] && hc < per_kv) val[j][c] = __ldg(src[j] + hc);
+                }
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int hc = base + c * 32 + lane;
+                if (hc >= per_kv) continue;
+                const int h = hc / chunks_per_row;
+                const long long off = h * tile + (hc - h * chunks_per_row);
+#pragma unroll
+                for (int j = 0; j < R; ++j)
+                    if (dst[j]) dst[j][off] = val[j][c];
+            }
+        }
     }
 }
 
@@ -124,14 +154,15 @@ extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_
         !aligned(status, 4))
         return PKV_E_ALIGN;
     const int chunks_per_row = desc->head_size / 8;
-    const long long total = (long long)num_tokens * 2 * desc->num_kv_heads * chunks_per_row;
-    const int threads = 256;
-    const long long want = (total + threads - 1) / threads;
+    const int threads = 256;  // 8 warps
+    const int per_kv = desc->num_kv_heads * chunks_per_row;
+    const int rows = per_kv >= 128 ? 1 : per_kv >= 64 ? 2 : 4;  // rows per warp and pass
+    const long long want = ((long long)num_tokens * 2 + 8 * rows - 1) / (8 * rows);
     const int blocks = (int)(want < (1 << 20) ? want : (1 << 20));
+    auto kernel = rows == 1 ? kv_write_kernel<1> : rows == 2 ? kv_write_kernel<2> : kv_write_kernel<4>;
     const cudaError_t err = launch_pdl(
-        kv_write_kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream),
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, (long long)num_tokens,
-        static_cast<uint4 *>(kv_cache), (long long)desc->num_blocks * PKV_BLOCK_SIZE, (int)desc->num_kv_heads,
-        chunks_per_row, status);
+        kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k),
+        static_cast<const uint4 *>(v), slot_mapping, (long long)num_tokens, static_cast<uint4 *>(kv_cache),
+        (long long)desc->num_blocks * PKV_BLOCK_SIZE, (int)desc->num_kv_heads, chunks_per_row, status);
     return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
