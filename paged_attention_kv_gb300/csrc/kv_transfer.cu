@@ -24,21 +24,32 @@ template <bool kGather>
 __global__ void __launch_bounds__(256) block_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                           const int32_t *__restrict__ block_ids, int num_ids,
                                                           long long vecs, int num_blocks, int32_t *status) {
+    // A CTA copies whole blocks (each one contiguous run of vecs 16-byte
+    // chunks), every thread with four loads in flight before its stores.
     pdl_launch_dependents();
     pdl_wait();
-    const long long total = (long long)num_ids * vecs;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long i = idx / vecs;
-        const long long v = idx - i * vecs;
+    constexpr int kUnroll = 4;
+    for (int i = blockIdx.x; i < num_ids; i += gridDim.x) {
         const int32_t b = __ldg(block_ids + i);
         if (b < 0 || b >= num_blocks) {
-            if (v == 0) raise_status(status, PKV_DEV_BAD_BLOCK);
+            if (threadIdx.x == 0) raise_status(status, PKV_DEV_BAD_BLOCK);
             continue;
         }
-        const long long pool = (long long)b * vecs + v, staged = i * vecs + v;
-        if (kGather) dst[staged] = __ldcs(src + pool);
-        else dst[pool] = __ldcs(src + staged);
+        const uint4 *s = src + (kGather ? (long long)b : (long long)i) * vecs;
+        uint4 *d = dst + (kGather ? (long long)i : (long long)b) * vecs;
+        for (long long base = threadIdx.x; base < vecs; base += (long long)blockDim.x * kUnroll) {
+            uint4 val[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const long long v = base + (long long)u * blockDim.x;
+                if (v < vecs) val[u] = __ldcs(s + v);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const long long v = base + (long long)u * blockDim.x;
+                if (v < vecs) d[v] = val[u];
+            }
+        }
     }
 }
 
@@ -53,9 +64,7 @@ int block_copy(const void *src, void *dst, const int32_t *block_ids, int32_t num
     if (!src || !dst || !block_ids) return PKV_E_NULL;
     if (!aligned(src, 16) || !aligned(dst, 16) || !aligned(block_ids, 4) || !aligned(status, 4)) return PKV_E_ALIGN;
     const long long vecs = 2LL * PKV_BLOCK_SIZE * desc->num_kv_heads * desc->head_size * 2 / 16;
-    const long long total = (long long)num_ids * vecs;
-    const long long want = (total + 255) / 256;
-    const int grid = (int)(want < (1 << 20) ? want : (1 << 20));
+    const int grid = num_ids < (1 << 20) ? num_ids : (1 << 20);  // a CTA per block
     const cudaError_t err = launch_pdl(block_copy_kernel<kGather>, dim3(grid), dim3(256), 0,
                                        static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(src),
                                        static_cast<uint4 *>(dst), block_ids, (int)num_ids, vecs,
