@@ -12,10 +12,12 @@
 //   softmax           sixteen warps, four per TMEM lane quadrant: a row is
 //                     one lane, its 128 keys split into four 32-key parts,
 //                     one per warp; the four partial row maxima meet in
-//                     shared memory. Causal mask, exp2 against a running
-//                     reference max that only moves (and rescales O) when a
-//                     row max grows by more than 2^8; P(x) goes to one of two
-//                     P buffers in TMEM as bf16 pairs;
+//                     shared memory (published before P is computed against
+//                     the current reference, collected after). Causal mask,
+//                     exp2 against a running reference max that only moves
+//                     (P redone, O rescaled) when a row max grows by more
+//                     than 2^8; P(x) goes to one of two P buffers in TMEM as
+//                     bf16 pairs;
 //   O += P(x) V(x)    tcgen05.mma (M=128, N=D) with A = P(x) read from TMEM
 //                     and B = V MN-major straight from its TMA tile; O stays
 //                     in TMEM.
