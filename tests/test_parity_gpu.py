@@ -420,6 +420,31 @@ def test_prepared_step_matches_the_checked_calls(workload):
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
 
 
+@pytest.mark.parametrize("hkv,d,tokens", [(3, 72, 37), (5, 80, 130), (1, 8, 300), (8, 128, 1000), (2, 256, 65)],
+                         ids=["27-chunk-rows", "50-chunk-rows", "1-chunk-rows", "128-chunk-rows", "64-chunk-rows"])
+def test_kv_write_row_widths_bit_exact(hkv, d, tokens):
+    """The KV write takes 1, 2 or 4 token rows per warp pass by row width
+    (hkv x d / 8 16-byte chunks); rows of every width class, ragged ones
+    included, land bit for bit where the oracle puts them, slots of -1 are
+    skipped and every other slot keeps its sentinel."""
+    rng = np.random.default_rng(hkv * 1000 + d)
+    nb = (tokens + 15) // 16 * 2
+    slots = rng.permutation(nb * 16)[:tokens].astype(np.int32)
+    slots[rng.random(tokens) < 0.1] = -1
+    g = torch.Generator().manual_seed(hkv + d)
+    k = torch.randn(tokens, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(tokens, hkv, d, generator=g).to(torch.bfloat16)
+    pool = torch.full((nb, 2, hkv, 16, d), float("nan"), dtype=torch.bfloat16)
+    ref = wl.bf16_bits(pool).copy()
+    oracle.kv_write(ref, wl.bf16_bits(k), wl.bf16_bits(v), slots)
+    dev_pool = pool.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write(k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), dev_pool, status)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(status) == 0
+    assert np.array_equal(wl.bf16_bits(dev_pool), ref)
+
+
 def test_a_wait_that_never_completes_is_reported_and_the_context_survives():
     """Failure detection without a fault: the self-test's wait on a barrier
     that nothing arrives on gives up after 2 ms, the status word carries
