@@ -44,10 +44,15 @@ PROFILE_DOC_CHUNK = os.path.join(REPO, "profiles", "chunk_kernel_mixed.md")
 
 
 def launches_per_step(batch) -> int:
-    """Slot mapping, KV write, work list, split-KV attention, and the chunk-tile
-    kernel whenever a 128-row tile can hold whole tokens of the batch."""
+    """Kernels one timed step launches (the prepared step): slot mapping with
+    the KV write (one launch), the work list, split-KV attention, and the
+    chunk-tile kernel when a request's new tokens can fill a 128-row tile
+    (the step passes its longest query to the library, which skips the
+    launch otherwise)."""
     g = batch.shape.num_q_heads // batch.shape.num_kv_heads
-    return 4 + (1 if 128 % g == 0 and batch.num_tokens * g >= 128 else 0)
+    longest = int(batch.query_lens.max()) if batch.num_reqs else 0
+    chunk = 128 % g == 0 and batch.num_tokens * g >= 128 and longest * g >= 128
+    return 3 + (1 if chunk else 0)
 
 
 def parse_args():

@@ -130,6 +130,18 @@ int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, in
                    void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream);
 
 /*
+ * paged_slot_mapping and paged_kv_write in one launch: each new token's slot
+ * is resolved from the tables (same rule, same status bits), stored in
+ * slot_mapping (device int32 [num_tokens], written) and used for that
+ * token's K/V at once. Same results as the two calls in sequence; one kernel
+ * launch fewer per step. Arguments as for those two calls.
+ */
+int paged_kv_write_slots(const void *k, const void *v, const int32_t *block_table, int32_t num_reqs,
+                         int32_t max_blocks_per_req, const int32_t *seq_lens, const int32_t *query_start_loc,
+                         int32_t num_tokens, void *kv_cache, const pkv_cache_desc *desc, int32_t *slot_mapping,
+                         int32_t *status, void *stream);
+
+/*
  * Block-granular KV transfer for disaggregated prefill/decode (page 1,
  * "Disaggregated P/D": the prefill instance uploads the KV it computed, and
  * before decoding, start_load_kv loads it and injects it into paged memory;
@@ -285,8 +297,8 @@ int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_head
  *   h2d stream:     one copy of slot s's packed inputs (host_in[s] ->
  *                   dev_in[s]), after the step that last used slot s has
  *                   finished its kernels;
- *   compute stream: paged_slot_mapping, paged_kv_write and
- *                   paged_attention_bounded on slot s's device arrays,
+ *   compute stream: paged_kv_write_slots and paged_attention_bounded on
+ *                   slot s's device arrays,
  *                   after that copy and after slot s's previous output has
  *                   left the device;
  *   d2h stream:     one copy of slot s's output to the caller's host

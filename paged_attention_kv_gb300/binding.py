@@ -37,7 +37,8 @@ PKV_DEV_BAD_SLOT = 0x8
 PKV_DEV_TIMEOUT = 0x10
 PKV_DEV_OVERFLOW = 0x20
 
-EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_gather_blocks",
+EXPORTED = ("pkv_kv_cache_bytes", "paged_slot_mapping", "paged_kv_write", "paged_kv_write_slots",
+            "paged_kv_gather_blocks",
             "paged_kv_scatter_blocks", "paged_attention_workspace_bytes",
             "paged_attention_min_workspace_bytes", "paged_attention", "paged_attention_timed",
             "paged_attention_bounded", "paged_attention_static", "pkv_pipeline_create", "pkv_pipeline_next",
@@ -82,6 +83,7 @@ def _load():
     lib.pkv_kv_cache_bytes.argtypes = [desc_p, ctypes.POINTER(sz)]
     lib.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
     lib.paged_kv_write.argtypes = [vp, vp, vp, i32, vp, desc_p, vp, vp]
+    lib.paged_kv_write_slots.argtypes = [vp, vp, vp, i32, i32, vp, vp, i32, vp, desc_p, vp, vp, vp]
     lib.paged_kv_gather_blocks.argtypes = [vp, desc_p, vp, i32, vp, vp, vp]
     lib.paged_kv_scatter_blocks.argtypes = [vp, vp, i32, vp, desc_p, vp, vp]
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, desc_p, ctypes.POINTER(sz)]
@@ -365,7 +367,7 @@ class StepBuffers:
         self.workspace = alloc_workspace(batch.num_reqs, self.num_tokens, batch.shape.num_q_heads, self.kv_cache)
 
     def prepared(self, stream=None) -> "PreparedStep":
-        """This step's three calls with their C arguments built once (for
+        """This step's calls with their C arguments built once (for
         loops that enqueue the same step many times: the per-call checks and
         argument conversion of the wrappers cost the host more than a small
         step costs the GPU). Valid while these buffers stay in place."""
@@ -383,8 +385,9 @@ class StepBuffers:
 
 class PreparedStep:
     """Slot mapping, KV write and attention of a StepBuffers, checked once,
-    then enqueued by calling the object: three C calls with prebuilt
-    arguments and no per-call Python checks."""
+    then enqueued by calling the object: two C calls (the fused slot mapping
+    and KV write, then attention) with prebuilt arguments and no per-call
+    Python checks."""
 
     def __init__(self, buf: "StepBuffers", stream=None):
         for t, dt, nd, name in ((buf.q, torch.bfloat16, 3, "q"), (buf.k, torch.bfloat16, 3, "k"),
@@ -405,14 +408,13 @@ class PreparedStep:
         st = _stream(stream)
         desc = ctypes.byref(self.desc)
         ws_bytes = ctypes.c_size_t(buf.workspace.numel() * buf.workspace.element_size())
+        if buf.k.shape[0] != buf.num_tokens:
+            raise ValueError("k must hold the step's num_tokens rows")
         self.calls = (
-            ("paged_slot_mapping", LIB.paged_slot_mapping,
-             (_ptr(buf.block_table), i32(r), i32(buf.block_table.shape[1]), _ptr(buf.seq_lens),
-              _ptr(buf.query_start_loc), i32(buf.num_tokens), i32(b.num_blocks), _ptr(buf.slot_mapping),
-              _ptr(buf.status), st)),
-            ("paged_kv_write", LIB.paged_kv_write,
-             (_ptr(buf.k), _ptr(buf.v), _ptr(buf.slot_mapping), i32(buf.k.shape[0]), _ptr(buf.kv_cache), desc,
-              _ptr(buf.status), st)),
+            ("paged_kv_write_slots", LIB.paged_kv_write_slots,
+             (_ptr(buf.k), _ptr(buf.v), _ptr(buf.block_table), i32(r), i32(buf.block_table.shape[1]),
+              _ptr(buf.seq_lens), _ptr(buf.query_start_loc), i32(buf.num_tokens), _ptr(buf.kv_cache), desc,
+              _ptr(buf.slot_mapping), _ptr(buf.status), st)),
             ("paged_attention_bounded", LIB.paged_attention_bounded,
              (_ptr(buf.q), i32(t), i32(hq), _ptr(buf.kv_cache), desc, _ptr(buf.block_table), i32(r),
               i32(buf.block_table.shape[1]), _ptr(buf.seq_lens), _ptr(buf.query_start_loc),

@@ -5,7 +5,8 @@
 //   h2d stream      [wait: slot's previous kernels]  copy host_in -> dev_in,
 //                   record loaded
 //   compute stream  [wait: loaded, slot's previous output copy]  slot
-//                   mapping, KV write, attention; record computed
+//                   mapping with the KV write (one launch), attention;
+//                   record computed
 //   d2h stream      [wait: computed]  copy out -> out_host, record returned
 // All buffers belong to the caller; the pipeline owns its events only.
 #include <cuda_runtime.h>
@@ -129,11 +130,8 @@ extern "C" PKV_API int pkv_pipeline_submit(pkv_pipeline *p, int32_t num_reqs, vo
     const int32_t *bt = reinterpret_cast<const int32_t *>(din + d.off_block_table);
     const int32_t *sl = reinterpret_cast<const int32_t *>(din + d.off_seq_lens);
     const int32_t *qsl = reinterpret_cast<const int32_t *>(din + d.off_query_start_loc);
-    int rc = paged_slot_mapping(bt, num_reqs, d.max_blocks_per_req, sl, qsl, d.num_tokens, d.cache.num_blocks,
-                                d.slot_mapping[s], d.status, comp);
-    if (!rc)
-        rc = paged_kv_write(din + d.off_k, din + d.off_v, d.slot_mapping[s], d.num_tokens, kv_cache, &d.cache,
-                            d.status, comp);
+    int rc = paged_kv_write_slots(din + d.off_k, din + d.off_v, bt, num_reqs, d.max_blocks_per_req, sl, qsl,
+                                  d.num_tokens, kv_cache, &d.cache, d.slot_mapping[s], d.status, comp);
     if (!rc)
         rc = paged_attention_bounded(din + d.off_q, d.num_tokens, d.num_q_heads, kv_cache, &d.cache, bt, num_reqs,
                                      d.max_blocks_per_req, sl, qsl, max_query_len, d.scale, d.out[s], d.workspace,

@@ -24,16 +24,11 @@ __device__ __forceinline__ int find_request(const int32_t *__restrict__ qsl, int
     return lo;
 }
 
-// One thread per new token.
-__global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int num_reqs, int max_blocks_per_req,
-                                    const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ qsl,
-                                    int num_tokens, int num_blocks, int32_t *__restrict__ slot_mapping,
-                                    int32_t *status) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t == 0 && (__ldg(qsl) != 0 || __ldg(qsl + num_reqs) != num_tokens)) raise_status(status, PKV_DEV_BAD_QSL);
-    if (t >= num_tokens) return;
+// Slot of new token t (-1 when its metadata is bad, which is reported).
+__device__ __forceinline__ int32_t token_slot(const int32_t *__restrict__ block_table, int num_reqs,
+                                              int max_blocks_per_req, const int32_t *__restrict__ seq_lens,
+                                              const int32_t *__restrict__ qsl, int num_blocks, int t,
+                                              int32_t *status) {
     const int r = find_request(qsl, num_reqs, t);
     const int q0 = __ldg(qsl + r), q1 = __ldg(qsl + r + 1);
     int32_t slot = -1;
@@ -51,8 +46,29 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int
             else slot = blk * PKV_BLOCK_SIZE + pos % PKV_BLOCK_SIZE;
         }
     }
-    slot_mapping[t] = slot;
+    return slot;
 }
+
+// One thread per new token.
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int num_reqs, int max_blocks_per_req,
+                                    const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ qsl,
+                                    int num_tokens, int num_blocks, int32_t *__restrict__ slot_mapping,
+                                    int32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t == 0 && (__ldg(qsl) != 0 || __ldg(qsl + num_reqs) != num_tokens)) raise_status(status, PKV_DEV_BAD_QSL);
+    if (t >= num_tokens) return;
+    slot_mapping[t] = token_slot(block_table, num_reqs, max_blocks_per_req, seq_lens, qsl, num_blocks, t, status);
+}
+
+// Where the KV write takes its slots from: the slot mapping (plain), or the
+// tables, resolving each token's slot on the way and storing it (fused).
+struct SlotSource {
+    const int32_t *block_table, *seq_lens, *qsl;
+    int num_reqs, max_blocks_per_req, num_blocks;
+    int32_t *slot_out;
+};
 
 // Each warp takes R adjacent (token, K or V) rows per pass: a row (the
 // token's K or V for all kv heads) is contiguous in k / v, and each head's D
@@ -60,13 +76,16 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int
 // worked out once per row; each lane then has R x (4 / R) = 4 16-byte loads
 // in flight before its stores (R = 1 for rows of >= 128 chunks, 4 for rows
 // of 32 or fewer).
-template <int R>
+template <int R, bool kFused>
 __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                 const int32_t *__restrict__ slot_mapping, long long num_tokens,
                                 uint4 *__restrict__ kv_cache, long long num_slots, int num_kv_heads,
-                                int chunks_per_row, int32_t *status) {
+                                int chunks_per_row, int32_t *status, const SlotSource src_tables) {
     pdl_launch_dependents();
     pdl_wait();
+    if (kFused && blockIdx.x == 0 && threadIdx.x == 0 &&
+        (__ldg(src_tables.qsl) != 0 || __ldg(src_tables.qsl + src_tables.num_reqs) != num_tokens))
+        raise_status(status, PKV_DEV_BAD_QSL);
     constexpr int C = 4 / R;  // chunks per lane per row and pass
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -84,7 +103,20 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__rest
             if (u >= units) continue;
             const long long t = u >> 1;
             const int kv = (int)(u & 1);
-            const int32_t slot = __ldg(slot_mapping + t);
+            int32_t slot;
+            if (kFused) {
+                // lane 0 resolves the slot (reporting bad metadata once, on the
+                // token's K row) and stores it; the warp shares it
+                int32_t s0 = 0;
+                if (lane == 0)
+                    s0 = token_slot(src_tables.block_table, src_tables.num_reqs, src_tables.max_blocks_per_req,
+                                    src_tables.seq_lens, src_tables.qsl, src_tables.num_blocks, (int)t,
+                                    kv == 0 ? status : nullptr);
+                slot = __shfl_sync(0xffffffffu, s0, 0);
+                if (lane == 0 && kv == 0) src_tables.slot_out[t] = slot;
+            } else {
+                slot = __ldg(slot_mapping + t);
+            }
             if (slot < 0) continue;
             if ((long long)slot >= num_slots) {
                 if (lane == 0 && kv == 0) raise_status(status, PKV_DEV_BAD_SLOT);
@@ -142,27 +174,67 @@ extern "C" PKV_API int paged_slot_mapping(const int32_t *block_table, int32_t nu
     return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
-extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
-                                      void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream) {
+namespace pkv {
+namespace {
+
+int kv_write_launch(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens, void *kv_cache,
+                    const pkv_cache_desc &desc, int32_t *status, void *stream, const SlotSource *fused) {
+    const int chunks_per_row = desc.head_size / 8;
+    const int threads = 256;  // 8 warps
+    const int per_kv = desc.num_kv_heads * chunks_per_row;
+    const int rows = per_kv >= 128 ? 1 : per_kv >= 64 ? 2 : 4;  // rows per warp and pass
+    const long long want = ((long long)num_tokens * 2 + 8 * rows - 1) / (8 * rows);
+    const int blocks = (int)(want < (1 << 20) ? want : (1 << 20));
+    const SlotSource none{};
+    auto kernel = fused ? (rows == 1 ? kv_write_kernel<1, true> : rows == 2 ? kv_write_kernel<2, true>
+                                                                            : kv_write_kernel<4, true>)
+                        : (rows == 1 ? kv_write_kernel<1, false> : rows == 2 ? kv_write_kernel<2, false>
+                                                                             : kv_write_kernel<4, false>);
+    const cudaError_t err = launch_pdl(
+        kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k),
+        static_cast<const uint4 *>(v), slot_mapping, (long long)num_tokens, static_cast<uint4 *>(kv_cache),
+        (long long)desc.num_blocks * PKV_BLOCK_SIZE, (int)desc.num_kv_heads, chunks_per_row, status,
+        fused ? *fused : none);
+    return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
+
+int check_kv_write_args(const void *k, const void *v, void *kv_cache, const pkv_cache_desc *desc, int32_t num_tokens,
+                        int32_t *status) {
     if (!desc) return PKV_E_NULL;
     int rc = check_cache_desc(*desc, /*attention=*/false);
     if (rc) return rc;
     if (num_tokens < 0) return PKV_E_DIMS;
     if (num_tokens == 0) return PKV_OK;
-    if (!k || !v || !slot_mapping || !kv_cache) return PKV_E_NULL;
-    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 4) ||
-        !aligned(status, 4))
+    if (!k || !v || !kv_cache) return PKV_E_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(kv_cache, 16) || !aligned(status, 4)) return PKV_E_ALIGN;
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" PKV_API int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
+                                      void *kv_cache, const pkv_cache_desc *desc, int32_t *status, void *stream) {
+    int rc = check_kv_write_args(k, v, kv_cache, desc, num_tokens, status);
+    if (rc || num_tokens == 0) return rc;
+    if (!slot_mapping) return PKV_E_NULL;
+    if (!aligned(slot_mapping, 4)) return PKV_E_ALIGN;
+    return kv_write_launch(k, v, slot_mapping, num_tokens, kv_cache, *desc, status, stream, nullptr);
+}
+
+extern "C" PKV_API int paged_kv_write_slots(const void *k, const void *v, const int32_t *block_table, int32_t num_reqs,
+                                            int32_t max_blocks_per_req, const int32_t *seq_lens,
+                                            const int32_t *query_start_loc, int32_t num_tokens, void *kv_cache,
+                                            const pkv_cache_desc *desc, int32_t *slot_mapping, int32_t *status,
+                                            void *stream) {
+    int rc = check_kv_write_args(k, v, kv_cache, desc, num_tokens, status);
+    if (rc || num_tokens == 0) return rc;
+    if (num_reqs <= 0 || max_blocks_per_req < 0) return PKV_E_DIMS;
+    if (!block_table || !seq_lens || !query_start_loc || !slot_mapping) return PKV_E_NULL;
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) ||
+        !aligned(slot_mapping, 4))
         return PKV_E_ALIGN;
-    const int chunks_per_row = desc->head_size / 8;
-    const int threads = 256;  // 8 warps
-    const int per_kv = desc->num_kv_heads * chunks_per_row;
-    const int rows = per_kv >= 128 ? 1 : per_kv >= 64 ? 2 : 4;  // rows per warp and pass
-    const long long want = ((long long)num_tokens * 2 + 8 * rows - 1) / (8 * rows);
-    const int blocks = (int)(want < (1 << 20) ? want : (1 << 20));
-    auto kernel = rows == 1 ? kv_write_kernel<1> : rows == 2 ? kv_write_kernel<2> : kv_write_kernel<4>;
-    const cudaError_t err = launch_pdl(
-        kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k),
-        static_cast<const uint4 *>(v), slot_mapping, (long long)num_tokens, static_cast<uint4 *>(kv_cache),
-        (long long)desc->num_blocks * PKV_BLOCK_SIZE, (int)desc->num_kv_heads, chunks_per_row, status);
-    return err == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    SlotSource src{block_table, seq_lens, query_start_loc, num_reqs, max_blocks_per_req, desc->num_blocks,
+                   slot_mapping};
+    return kv_write_launch(k, v, nullptr, num_tokens, kv_cache, *desc, status, stream, &src);
 }

@@ -156,3 +156,24 @@ def test_pipeline_create_validates_the_description_before_any_cuda_call():
     assert pkv.LIB.pkv_pipeline_submit(None, 1, None, None, -1) == pkv.PKV_E_NULL
     assert pkv.LIB.pkv_pipeline_sync(None) == pkv.PKV_E_NULL
     assert pkv.LIB.pkv_pipeline_destroy(None) == pkv.PKV_OK
+
+
+def test_fused_kv_write_host_validation():
+    vp = ctypes.c_void_p
+    f = pkv.LIB.paged_kv_write_slots
+    d = ctypes.byref(_desc())
+    ok = dict(k=vp(0x1000), v=vp(0x2000), bt=vp(0x3000), sl=vp(0x4000), qsl=vp(0x5000), kv=vp(0x6000),
+              slots=vp(0x7000))
+
+    def call(r=2, mbr=3, t=4, desc=d, **kw):
+        a = {**ok, **kw}
+        return f(a["k"], a["v"], a["bt"], r, mbr, a["sl"], a["qsl"], t, a["kv"], desc, a["slots"], None, None)
+    assert call(t=0) == pkv.PKV_OK
+    assert call(k=None) == pkv.PKV_E_NULL
+    assert call(slots=None) == pkv.PKV_E_NULL
+    assert call(qsl=None) == pkv.PKV_E_NULL
+    assert call(k=vp(0x1004)) == pkv.PKV_E_ALIGN
+    assert call(bt=vp(0x3002)) == pkv.PKV_E_ALIGN
+    assert call(r=0) == pkv.PKV_E_DIMS
+    assert call(t=-1) == pkv.PKV_E_DIMS
+    assert call(desc=ctypes.byref(_desc(bs=32))) == pkv.PKV_E_BLOCK_SIZE

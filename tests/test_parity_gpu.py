@@ -445,6 +445,41 @@ def test_kv_write_row_widths_bit_exact(hkv, d, tokens):
     assert np.array_equal(wl.bf16_bits(dev_pool), ref)
 
 
+def test_fused_slot_mapping_and_kv_write_match_the_two_calls():
+    """paged_kv_write_slots gives the slot mapping, pool and status bits of
+    paged_slot_mapping followed by paged_kv_write, including a token whose
+    block-table entry is out of range (flagged, its K/V skipped)."""
+    batch = _custom(LLAMA, [300, 17, 700, 64], [5, 1, 200, 64], 670)
+    ten = device_tensors(batch, generate_on="cpu")
+    bt = batch.block_table.copy()
+    bt[1, 1] = batch.num_blocks + 5  # request 1's new token (position 16) lands in block slot 1
+    dev = {k: v.clone() for k, v in ten.items()}
+    bt_d = torch.from_numpy(bt).cuda()
+    sl_d = torch.from_numpy(batch.seq_lens).cuda()
+    qsl_d = torch.from_numpy(batch.query_start_loc).cuda()
+    t = batch.num_tokens
+    st_a = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots_a = pkv.paged_slot_mapping(bt_d, sl_d, qsl_d, t, batch.num_blocks, status=st_a)
+    pool_a = dev["kv_cache"].clone()
+    pkv.paged_kv_write(dev["k"], dev["v"], slots_a, pool_a, st_a)
+    st_b = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots_b = torch.full((t,), 12345, dtype=torch.int32, device="cuda")
+    pool_b = dev["kv_cache"].clone()
+    desc = pkv.cache_desc(pool_b)
+    import ctypes
+    vp = ctypes.c_void_p
+    rc = pkv.LIB.paged_kv_write_slots(vp(dev["k"].data_ptr()), vp(dev["v"].data_ptr()), vp(bt_d.data_ptr()),
+                                      batch.num_reqs, bt.shape[1], vp(sl_d.data_ptr()), vp(qsl_d.data_ptr()), t,
+                                      vp(pool_b.data_ptr()), ctypes.byref(desc), vp(slots_b.data_ptr()),
+                                      vp(st_b.data_ptr()), vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(st_a) == pkv.pkv_read_status(st_b) == pkv.PKV_DEV_BAD_BLOCK
+    assert torch.equal(slots_a, slots_b)
+    assert int(slots_b[5].item()) == -1
+    assert torch.equal(pool_a.view(torch.int16), pool_b.view(torch.int16))
+
+
 def test_a_wait_that_never_completes_is_reported_and_the_context_survives():
     """Failure detection without a fault: the self-test's wait on a barrier
     that nothing arrives on gives up after 2 ms, the status word carries
