@@ -49,6 +49,9 @@ struct PlanArgs {
     int num_reqs, num_tokens, max_blocks_per_req, group, num_kv_heads;
     int block_bytes_kv;  // K + V bytes of one (block, kv head): 2 * 16 * D * 2
     int chunk_ok;        // the tcgen05 chunk kernel can take this shape (128 % g == 0)
+    int sm_count;
+    float chunk_sm_us_per_tile;  // SM-microseconds one 128 x 128 chunk tile step costs
+    float decode_bytes_per_us;   // split-KV streaming rate of the whole GPU
     long long target_items, part_rows_cap, groups_cap, items_cap, chunk_items_cap;
     WsHeader *header;
     int32_t *req_cache;  // kReqCacheArrays * (num_reqs + 1) ints, when the batch has too many requests for shared memory
@@ -492,6 +495,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) a.header->n_partial_rows = row_carry;
 
     // 5. chunk items, longest first.
+    long long csteps = 0;  // (item, 128-key tile) steps of the chunk kernel
     for (int base = 0; base < n_cgroups; base += kPlanThreads) {
         const int gi = base + tid;
         int r = 0, mt = 0, kv_end = 0, b = -1;
@@ -503,6 +507,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         }
         const int first = (b >= 0 ? s_cbucket_base[b] : 0) + warp_claim(b, Hkv, s_cbucket_cursor);
         if (gi >= n_cgroups) continue;
+        csteps += (long long)((kv_end + kChunkKeys - 1) / kChunkKeys) * Hkv;
         const int n = req_n[r];
         const long long rows = (long long)n * g;
         const int nv = (int)min((long long)kChunkRows, rows - (long long)mt * kChunkRows);
@@ -513,6 +518,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             c.b = make_int4(req_q0[r], n, req_L[r], nv);
             a.chunk_items[idx] = c;
         }
+    }
+    // 6. The chunk kernel's share of the SMs when it runs beside the
+    // split-KV kernel: about what makes its tiles take as long as the split-KV
+    // stream, capped so the stream keeps the SMs it needs to saturate HBM.
+    if (n_cgroups > 0) csteps = block_sum<long long>(csteps, s_ll);  // n_cgroups is the same in every thread
+    if (tid == 0) {
+        int ctas = 0;
+        if (csteps > 0) {
+            const double chunk_sm_us = (double)csteps * a.chunk_sm_us_per_tile;
+            const double decode_us = (double)work * a.block_bytes_kv / a.decode_bytes_per_us;
+            if (decode_us < 1.0) {
+                ctas = a.sm_count;
+            } else {
+                ctas = (int)ceil(chunk_sm_us / decode_us);
+                ctas = max(1, min(ctas, a.sm_count * 9 / 20));
+            }
+        }
+        a.header->chunk_ctas = ctas;
     }
 }
 
@@ -534,6 +557,7 @@ struct DecodeArgs {
     int32_t *tile_counter;
     float2 *part_ml;
     float *part_o;
+    int beside_chunk;  // launched after the chunk kernel, running beside it (see attention_impl)
 };
 
 // Per-item description handed from the producer to the consumers through
@@ -1084,8 +1108,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     }
     __syncthreads();
     // The prologue above overlaps the previous kernel; the work list it
-    // wrote is read only after this.
-    pdl_wait();
+    // wrote is read only after this. Beside the chunk kernel, the previous
+    // kernel is the chunk kernel, which launched this one only after the
+    // work list was complete; this kernel waits for it at its end instead.
+    if (!a.beside_chunk) pdl_wait();
     pdl_launch_dependents();
     const int n_prefix = a.header->n_prefix_items;
     const int n_items = n_prefix + a.header->n_items;
@@ -1141,7 +1167,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         // they leave together and never strand each other at a barrier.
         if (tid == 0) s_stop = (!have_q || *abort || d.item < 0) ? 1 : 0;
         named_barrier_sync(1, kConsumerWarps * 32);
-        if (s_stop) return;
+        if (s_stop) {
+            // beside the chunk kernel: end only after it (one thread holds the CTA)
+            if (a.beside_chunk && tid == 0) pdl_wait();
+            return;
+        }
 
         // Up to 4 rows (a decode token's GQA group of 4 or fewer): the
         // transposed 8-row products; more: 16-row products, whose shorter
@@ -1261,6 +1291,19 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+
+// SM-microseconds one 128 x 128 chunk tile step is costed at when the work
+// list shares the SMs between the chunk and split-KV kernels. Measured on
+// GB300: ~1.8 at head 128 (the mixed batch's 4352 steps in ~52 us on 152
+// SMs); the mixed step was flat from 1.8 to 3.6 (the split-KV stream was the
+// longer side) and 35 % slower at 1.2, so the value sits inside that range.
+// Head 64 is scaled the same way, not measured.
+#ifndef PKV_CHUNK_SM_US_128
+#define PKV_CHUNK_SM_US_128 2.8f
+#endif
+#ifndef PKV_CHUNK_SM_US_64
+#define PKV_CHUNK_SM_US_64 1.9f
+#endif
 
 struct DeviceInfo {
     int sm_count = 0;
@@ -1453,6 +1496,9 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     pa.num_kv_heads = Hkv;
     pa.block_bytes_kv = 2 * PKV_BLOCK_SIZE * D * 2;
     pa.chunk_ok = chunk_ok ? 1 : 0;
+    pa.sm_count = di->sm_count;
+    pa.chunk_sm_us_per_tile = D == 128 ? PKV_CHUNK_SM_US_128 : PKV_CHUNK_SM_US_64;  // the split-KV stream: ~6.8 TB/s
+    pa.decode_bytes_per_us = 6.8e6f;
     pa.chunk_items_cap = L.chunk_items_cap;
     pa.chunk_items = reinterpret_cast<ChunkItem *>(ws + L.chunk_items);
     pa.target_items = (long long)ctas * kItemsPerCta;
@@ -1478,7 +1524,7 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     if (err != cudaSuccess) return PKV_E_CUDA;
     record(events, 1, st);
 
-    DecodeArgs da;
+    DecodeArgs da{};
     da.q = static_cast<const __nv_bfloat16 *>(q);
     da.out = static_cast<__nv_bfloat16 *>(out);
     da.block_table = block_table;
@@ -1497,8 +1543,14 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
     da.part_ml = reinterpret_cast<float2 *>(ws + L.part_ml);
     da.part_o = reinterpret_cast<float *>(ws + L.part_o);
 
+    auto launch_decode = [&]() {
+        return D == 128 ? launch_pdl(decode_kernel<128>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<128>::kAlloc,
+                                     st, kv_map, da)
+                        : launch_pdl(decode_kernel<64>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<64>::kAlloc,
+                                     st, kv_map, da);
+    };
+    ChunkArgs ca{};
     if (chunk_ok) {
-        ChunkArgs ca;
         ca.block_table = block_table;
         ca.max_blocks_per_req = max_blocks_per_req;
         ca.num_blocks = desc->num_blocks;
@@ -1509,13 +1561,21 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.items = pa.chunk_items;
         ca.header = header;
         ca.out = static_cast<__nv_bfloat16 *>(out);
-        if (chunk_launch(D, di->sm_count, kv_map_chunk, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     }
+    // With chunk tiles (and no per-kernel timing), the chunk kernel runs
+    // beside the split-KV kernel: its CTAs past the work list's share leave
+    // at once, and the split-KV kernel (which may launch only once every
+    // chunk CTA has started or left) fills the SMs they free. The split-KV
+    // kernel then reads the work list without waiting for the chunk kernel
+    // and waits for it only at its end, so later work on `st` still starts
+    // after both.
+    if (chunk_ok && !events) {
+        ca.beside = 1;
+        da.beside_chunk = 1;
+    }
+    if (chunk_ok && chunk_launch(D, di->sm_count, kv_map_chunk, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     record(events, 2, st);
-    if (D == 128)
-        err = launch_pdl(decode_kernel<128>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<128>::kAlloc, st, kv_map, da);
-    else
-        err = launch_pdl(decode_kernel<64>, dim3(ctas), dim3(kDecodeThreads), DecodeSmem<64>::kAlloc, st, kv_map, da);
+    err = launch_decode();
     record(events, 3, st);
     return err == cudaSuccess && cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }

@@ -172,7 +172,9 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     pdl_wait();
     pdl_launch_dependents();
     const int n_items = a.header->n_chunk_items;
-    if (n_items == 0) return;
+    // Beside the split-KV kernel, CTAs past the work list's share leave
+    // their SMs to it at once.
+    if (n_items == 0 || (a.beside && (int)blockIdx.x >= a.header->chunk_ctas)) return;
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tmem_fence_before_sync();
     __syncthreads();

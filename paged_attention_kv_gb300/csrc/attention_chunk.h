@@ -24,6 +24,7 @@ struct ChunkArgs {
     const ChunkItem *items;
     WsHeader *header;
     __nv_bfloat16 *out;
+    int beside;  // running beside the split-KV kernel: only the first header->chunk_ctas CTAs work
 };
 
 int chunk_smem_bytes(int head_size);

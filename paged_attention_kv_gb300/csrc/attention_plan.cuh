@@ -73,7 +73,8 @@ struct WsHeader {
     int32_t diag;          // bits naming the pipeline waits that timed out (PKV_DEV_TIMEOUT)
     int32_t n_prefix_items; // prefix-tile items (listed before the split items; 0 without a shared prefix)
     int32_t cascade_blocks; // P: leading blocks shared by every request (0: none)
-    int32_t pad[53];
+    int32_t chunk_ctas;     // chunk-kernel CTAs that stay when it runs beside the split-KV kernel
+    int32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
