@@ -523,3 +523,43 @@ def test_duplicate_slots_stay_inside_their_slot():
         ok = np.all(got == a0, axis=2) | np.all(got == a1, axis=2)
         assert ok.all()
         assert np.array_equal(after[9, kv, :, 1, :], src[2])
+
+
+@pytest.mark.parametrize("case", ["mixed", "chunk_heavy", "chunk_only"])
+def test_chunk_kernel_beside_split_kv_gives_the_serial_bits(case):
+    """With chunk tiles, the chunk kernel runs beside the split-KV kernel on
+    the share of the SMs the work list sets (all of them when the decode part
+    is negligible); with timing events the two run one after the other. Both
+    orders must give the same bits (each output row is computed by one kernel
+    in a fixed order), within tolerance of the oracle, and the share must lie
+    in [1, SMs]."""
+    if case == "mixed":
+        batch = wl.make_batch("mixed")
+    elif case == "chunk_heavy":  # long prefill chunks beside a handful of short decodes
+        batch = _custom(LLAMA, [4096, 3000, 64, 200, 33], [2048, 1024, 1, 1, 1], 671)
+    else:  # no split-KV rows at all
+        batch = _custom(TINY, [1024, 700], [512, 256], 672)
+    ten = device_tensors(batch, generate_on="cpu")
+    host = host_inputs(ten)
+    slots, pool, ref = oracle_step(batch, host)
+    buf = pkv.StepBuffers(batch, ten)
+    buf.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(buf.status) == 0 and pkv.pkv_read_status(buf.workspace) == 0
+    beside = buf.out.clone()
+    h = buf.workspace[:16].view(torch.int32).cpu().numpy()
+    n_chunk_items, chunk_ctas = int(h[6]), int(h[11])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert n_chunk_items > 0
+    assert 1 <= chunk_ctas <= sms, chunk_ctas
+    if case != "mixed":
+        assert chunk_ctas == sms  # the split-KV side is under a microsecond
+    assert_attention_close(beside, ref, what=f"{case} beside")
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    buf.out.zero_()
+    pkv.paged_attention(buf.q, buf.kv_cache, buf.block_table, buf.seq_lens, buf.query_start_loc, batch.scale,
+                        buf.out, buf.workspace, events=ev)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(buf.workspace) == 0
+    assert torch.equal(beside.view(torch.int16), buf.out.view(torch.int16))
