@@ -575,6 +575,13 @@ struct ItemDesc {
     int row_arr[kRowsPerTile];   // arrivals that tile waits for
 };
 
+// Blocks before an item's last copy at which the producer claims its CTA's
+// next item. Same-box sweep on GB300 (Llama-3-8B decode step): claimed at the
+// item's start 340.2 us; 8 blocks ahead 339.1; 16: 337.6; 32: 336.3; 64: 338.7.
+#ifndef PKV_CLAIM_AHEAD
+#define PKV_CLAIM_AHEAD 32
+#endif
+
 template <int D>
 struct DecodeSmem {
     static constexpr int kBoxes = D / 64;                   // 64-column TMA boxes per tile
@@ -611,7 +618,7 @@ __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, 
 template <int D, bool kPrefix>
 __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const DecodeArgs &a, uint8_t *smem, ItemDesc &d,
                                              int qb, int cur, int n_prefix, int split, int P, uint64_t *bar,
-                                             uint32_t &e, int32_t *status, volatile int *abort) {
+                                             uint32_t &e, int32_t *status, volatile int *abort, int &nxt) {
     using S = DecodeSmem<D>;
     uint64_t *full = bar, *empty = bar + S::kStages, *qfull = bar + 2 * S::kStages;
     const int lane = threadIdx.x & 31;
@@ -701,11 +708,20 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
         }
         return b;
     };
+    // The CTA's next item is claimed PKV_CLAIM_AHEAD blocks before this
+    // one's last copy is issued: late enough that a CTA never holds a whole
+    // item in reserve while others run dry at the end of the list, early
+    // enough that the claim's round trip is hidden.
+    bool claimed = false;
     int my_blk = fetch(kb0);
     for (int base = kb0; base < kb1 && ok; base += 32) {
         const int nxt_blk = fetch(base + 32);
         const int cnt = min(32, kb1 - base);
         for (int j = 0; j < cnt; ++j) {
+            if (!claimed && kb1 - (base + j) <= PKV_CLAIM_AHEAD) {
+                if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);
+                claimed = true;
+            }
             const int blk = __shfl_sync(0xffffffffu, my_blk, j);
             const int stage = e % S::kStages;
             if (!mbar_wait(&empty[stage], ((e / S::kStages) & 1) ^ 1, status, abort)) { ok = false; break; }
@@ -719,6 +735,7 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
         }
         my_blk = nxt_blk;
     }
+    if (!claimed && lane == 0) nxt = atomicAdd(&a.header->next_item, 1);
     return ok;
 }
 
@@ -803,10 +820,15 @@ __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem,
             __syncwarp();
         }
 
-        // S^T = K Q^T: A = the block's 16 keys x 16 columns per K step.
-        float sc[NT][4];
+        // S^T = K Q^T: A = the block's 16 keys x 16 columns per K step; even
+        // and odd K steps accumulate apart (two dependency chains of half
+        // the length), then add.
+        float sc[NT][4], sc2[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+        }
         {
             const int key = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -815,9 +837,15 @@ __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem,
                 uint32_t ka[4];
                 ldmatrix_x4(kbase + (chunk >> 3) * 2048 + swz128(key, chunk & 7), ka[0], ka[1], ka[2], ka[3]);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], ka, qf[kk][nt][0], qf[kk][nt][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816((kk & 1) ? sc2[nt] : sc[nt], ka, qf[kk][nt][0], qf[kk][nt][1]);
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[nt][c] += sc2[nt][c];
         }
+
 
         // Scale into the log2 domain, causal mask, online softmax per row
         // (a column of S^T: keys gid and gid + 8 here, the rest across the
@@ -1135,12 +1163,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
                 mbar_arrive(&qfull[qb]);
                 break;
             }
-            int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);  // next item, fetched early
+            int nxt = 0;  // lane 0: the next item, claimed inside produce_item
             ok = cur < n_prefix
-                     ? produce_item<D, true>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status, abort)
+                     ? produce_item<D, true>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status,
+                                             abort, nxt)
                      : produce_item<D, false>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status,
-                                              abort);
+                                              abort, nxt);
             if (!ok) break;
             cur = __shfl_sync(0xffffffffu, nxt, 0);
         }
