@@ -558,6 +558,7 @@ struct DecodeArgs {
     float2 *part_ml;
     float *part_o;
     int beside_chunk;  // launched after the chunk kernel, running beside it (see attention_impl)
+    int static_first;  // CTA b starts on item b (the batch's rows promise at least one item per CTA)
 };
 
 // Per-item description handed from the producer to the consumers through
@@ -618,7 +619,8 @@ __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, 
 template <int D, bool kPrefix>
 __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const DecodeArgs &a, uint8_t *smem, ItemDesc &d,
                                              int qb, int cur, int n_prefix, int split, int P, uint64_t *bar,
-                                             uint32_t &e, int32_t *status, volatile int *abort, int &nxt) {
+                                             uint32_t &e, int32_t *status, volatile int *abort, int claim_base,
+                                             int &nxt) {
     using S = DecodeSmem<D>;
     uint64_t *full = bar, *empty = bar + S::kStages, *qfull = bar + 2 * S::kStages;
     const int lane = threadIdx.x & 31;
@@ -719,7 +721,7 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
         const int cnt = min(32, kb1 - base);
         for (int j = 0; j < cnt; ++j) {
             if (!claimed && kb1 - (base + j) <= PKV_CLAIM_AHEAD) {
-                if (lane == 0) nxt = atomicAdd(&a.header->next_item, 1);
+                if (lane == 0) nxt = claim_base + atomicAdd(&a.header->next_item, 1);
                 claimed = true;
             }
             const int blk = __shfl_sync(0xffffffffu, my_blk, j);
@@ -735,7 +737,7 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
         }
         my_blk = nxt_blk;
     }
-    if (!claimed && lane == 0) nxt = atomicAdd(&a.header->next_item, 1);
+    if (!claimed && lane == 0) nxt = claim_base + atomicAdd(&a.header->next_item, 1);
     return ok;
 }
 
@@ -746,9 +748,9 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
 // The products run transposed, with the query rows as the mma's N = 8
 // dimension: S^T (16 keys x 8 rows) = K Q^T and O^T (D x 8 rows) += V^T P^T.
 // One 8-row n-tile (NT = 1) costs half the mma instructions of a 16-row
-// tile, most of whose rows are padding for a decode token's GQA group of 4;
-// with 16-row products the legacy mma path sets a per-block rate about equal
-// to the HBM rate itself. P^T goes from the accumulator layout to the B
+// tile, half or more of whose rows are padding for a decode token's GQA
+// group of 4 or 8; the legacy mma path's rate per SM is what bounds a
+// consumer warp's per-block time. P^T goes from the accumulator layout to the B
 // operand layout with two 8x8 register transposes (movmatrix).
 template <int D, int NT>
 __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem, const ItemDesc &d, int qb,
@@ -940,7 +942,7 @@ __device__ __forceinline__ void consume_item(const DecodeArgs &a, uint8_t *smem,
     }
 }
 
-// One consumer warp's share of an item with more than 4 valid rows: its
+// One consumer warp's share of an item with more than 8 valid rows: its
 // blocks against all 16 rows of the tile (S = Q K^T, O += P V with the rows
 // as M = 16), then its unnormalised O, running max and sum per row into the
 // CTA's scratch.
@@ -1151,9 +1153,18 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         if (lane == 0) tma_prefetch_desc(&kv_map);
         uint32_t e = 0;  // ring element counter
         bool ok = true;
-        int cur = 0;
-        if (lane == 0) cur = atomicAdd(&a.header->next_item, 1);
-        cur = __shfl_sync(0xffffffffu, cur, 0);
+        // When the batch has about one item per CTA or more, CTA b starts on
+        // item b (the list is longest first, so the longest items spread
+        // over the SMs) and later items come from the counter, past the
+        // grid's first items (a CTA whose b is past the list just leaves).
+        // Otherwise, and beside the chunk kernel (where some CTAs start only
+        // when chunk CTAs leave), every item is claimed from the counter.
+        const int claim_base = a.static_first ? (int)gridDim.x : 0;
+        int cur = (int)blockIdx.x;
+        if (!a.static_first) {
+            if (lane == 0) cur = atomicAdd(&a.header->next_item, 1);
+            cur = __shfl_sync(0xffffffffu, cur, 0);
+        }
         for (int k = 0;; ++k) {
             const int qb = k & 1;
             if (!mbar_wait(&qempty[qb], ((k >> 1) & 1) ^ 1, status, abort)) { ok = false; break; }
@@ -1166,9 +1177,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             int nxt = 0;  // lane 0: the next item, claimed inside produce_item
             ok = cur < n_prefix
                      ? produce_item<D, true>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status,
-                                             abort, nxt)
+                                             abort, claim_base, nxt)
                      : produce_item<D, false>(&kv_map, a, smem, desc[qb], qb, cur, n_prefix, split, P, bar, e, status,
-                                              abort, nxt);
+                                              abort, claim_base, nxt);
             if (!ok) break;
             cur = __shfl_sync(0xffffffffu, nxt, 0);
         }
@@ -1201,10 +1212,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             return;
         }
 
-        // Up to 4 rows (a decode token's GQA group of 4 or fewer): the
-        // transposed 8-row products; more: 16-row products, whose shorter
-        // per-block dependency chain matters more than their padding.
-        if (d.n_valid <= 4)
+        // Up to 8 rows (a decode token's GQA group of 8 or fewer): the
+        // transposed 8-row products, half the mma instructions of 16-row
+        // ones; more: 16-row products.
+        if (d.n_valid <= 8)
             consume_item<D, 1>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
         else
             consume_item16<D>(a, smem, d, qb, full, empty, e, status, abort, warp, lane, scr, sml);
@@ -1601,6 +1612,12 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.beside = 1;
         da.beside_chunk = 1;
     }
+    // Every 16 rows of a kv head make at least one split-KV item, so this
+    // many rows promise an item per CTA (rows the chunk kernel takes count
+    // too: a wrong guess only leaves some CTAs idle at first, never a wrong
+    // result). Deciding on the host spares the CTAs a dependent read of the
+    // work list's item count before their first claim.
+    da.static_first = !da.beside_chunk && ((long long)num_tokens * da.group / kRowsPerTile) * Hkv >= ctas ? 1 : 0;
     if (chunk_ok && chunk_launch(D, di->sm_count, kv_map_chunk, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     record(events, 2, st);
     err = launch_decode();
