@@ -113,6 +113,13 @@ __device__ __forceinline__ int tile_kv_end(int n, int L, int g, int mt) {
     return L - n + (int)(last_row / g) + 1;
 }
 
+// Device-scope atomic add with acquire-release ordering; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel(int32_t *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int tile_rows(int n, int g, int mt) {
     return (int)min((long long)kRowsPerTile, (long long)n * g - (long long)mt * kRowsPerTile);
 }
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             if (pl.w > 1) a.tile_counter[gq * Hkv + h] = 0;
             for (int s = 0; s < ns_g; ++s) {
                 const long long idx = s < ns_g - 1 ? (long long)pl.x + h * (ns_g - 1) + s : (long long)pl.y + h;
-                if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, 0);
+                if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, grp_req[gq]);
             }
         }
         __syncthreads();
@@ -632,6 +639,8 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
     const int Hkv = a.num_kv_heads, g = a.group;
     bool ok = true;
     int r, mt, q0, nv, kb0, kb1, kv_end, h;
+    const int32_t *early_bt = nullptr;  // split items: block table row and first entries read early
+    int early_raw = 0;
     if constexpr (kPrefix) {
         // Prefix tile: global rows [pt * 16, +16) over the shared
         // blocks [0, P), which every row sees whole.
@@ -656,12 +665,17 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
         const int4 w = a.items[cur - n_prefix].v;
         const int gi = w.x, s = w.z;
         h = w.y;
+        // The item names its request, so the first 32 block-table entries
+        // are requested together with the group record, not after it; they
+        // are checked against the item's block range below.
+        kb0 = P + s * split;
+        early_bt = a.block_table + (long long)w.w * a.max_blocks_per_req;
+        early_raw = kb0 + lane < a.max_blocks_per_req ? __ldg(early_bt + kb0 + lane) : 0;
         const GroupRec G = a.group_rec[gi];
         r = G.a.x; mt = G.a.y; q0 = G.a.z;
         const int n = G.a.w, L = G.b.x, kvb = G.b.z, slots = G.c.z;
         nv = G.b.w;
         kv_end = G.b.y;
-        kb0 = P + s * split;
         kb1 = min(kvb, kb0 + split);
         // Rows: token, q head, last visible key, partial row.
         if (lane < kRowsPerTile) {
@@ -720,7 +734,19 @@ __device__ __forceinline__ bool produce_item(const CUtensorMap *kv_map, const De
     // item in reserve while others run dry at the end of the list, early
     // enough that the claim's round trip is hidden.
     bool claimed = false;
-    int my_blk = fetch(kb0);
+    int my_blk;
+    if (!kPrefix && early_bt == bt) {
+        my_blk = 0;
+        if (kb0 + lane < kb1) {
+            my_blk = early_raw;
+            if (my_blk < 0 || my_blk >= a.num_blocks) {
+                raise_status(status, PKV_DEV_BAD_BLOCK);
+                my_blk = a.num_blocks;
+            }
+        }
+    } else {
+        my_blk = fetch(kb0);
+    }
     for (int base = kb0; base < kb1 && ok; base += 32) {
         const int nxt_blk = fetch(base + 32);
         const int cnt = min(32, kb1 - base);
@@ -1263,22 +1289,24 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
             // Publish the partial rows, then count one arrival at each tile
             // they belong to (the first row of each run of equal tiles
             // counts); the CTA that brings a tile's count to its arrivals
-            // merges the tile (no waiting).
-            __threadfence();
+            // merges the tile (no waiting). The count is an acquire-release
+            // atomic after the consumers' barrier: it releases every
+            // consumer thread's partial rows, and for the last arriver it
+            // acquires the other CTAs' rows, which its threads read after
+            // the next barrier.
             named_barrier_sync(1, kConsumerWarps * 32);
             if (warp == 0) {
                 bool last = false;
                 if (lane < n_valid) {
                     const int tile = d.row_tile[lane];
                     if (lane == 0 || d.row_tile[lane - 1] != tile)
-                        last = atomicAdd(&a.tile_counter[tile], 1) == d.row_arr[lane] - 1;
+                        last = atom_add_acq_rel(&a.tile_counter[tile], 1) == d.row_arr[lane] - 1;
                 }
                 const unsigned mask = __ballot_sync(0xffffffffu, last);
                 if (lane == 0) s_last = (int)mask;
             }
             named_barrier_sync(1, kConsumerWarps * 32);
             unsigned todo = (unsigned)s_last;
-            if (todo) __threadfence();
             while (todo) {
                 const int tile = d.row_tile[__ffs(todo) - 1];
                 todo &= todo - 1;

@@ -78,8 +78,10 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// One split-KV work item: {group, kv head h, split s, 0}. The rest lives in
-// the group's record, written once per group.
+// One split-KV work item: {group, kv head h, split s, request}. The rest
+// lives in the group's record, written once per group; the request is here
+// too so that the attention kernel can read its block-table row while the
+// group record is on its way.
 struct WorkItem {
     int4 v;
 };
