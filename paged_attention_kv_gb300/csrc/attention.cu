@@ -2,16 +2,21 @@
 // forward pass" step 3: one super sequence, each sequence attending only to
 // its own tokens; decode and chunked-prefill requests mixed in one step).
 //
-// Two launches on the caller's stream:
+// Up to three launches on the caller's stream:
 //   plan_kernel    one CTA turns query_start_loc / seq_lens into a work list
 //                  (attention_plan.cuh): it picks the split-KV length so the
 //                  persistent grid gets ~kItemsPerCta items per CTA and lists
 //                  the items longest first;
+//   chunk_kernel   (attention_chunk.cu) the 128-row tensor-core tiles of
+//                  requests with many new tokens, on a share of the SMs
+//                  beside the next kernel; skipped when no request can fill
+//                  a tile;
 //   decode_kernel  persistent, warp-specialised. One producer warp takes
 //                  items from an atomic counter, bulk-copies each item's Q
-//                  rows and gathers each K/V block tile (16 rows x D,
-//                  contiguous in the pool) with TMA into a shared-memory
-//                  ring; four consumer warps run S = Q K^T and O += P V on
+//                  rows and gathers each (block, kv head)'s K and V rows (16
+//                  x D each, contiguous in the pool) with one TMA box into a
+//                  shared-memory ring; four consumer warps run S = Q K^T and
+//                  O += P V on
 //                  bf16 mma.sync tensor-core tiles with an fp32 online
 //                  softmax (exp2 domain), combine their states in shared
 //                  memory, and either write the output or a split partial;
