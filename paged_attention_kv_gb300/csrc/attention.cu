@@ -423,6 +423,95 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         s_n_chunk_items = cacc;
     }
     __syncthreads();
+
+    // 4. partial-row bases (chunked scan over groups) and the decode items.
+    // Per chunk of kPlanThreads groups (thread tid = group base + tid): the
+    // scan, the items' places and the group record, in registers and shared
+    // memory only (compute4); then the workspace writes (write4). When every
+    // group fits in one chunk and the tables live in shared memory, compute4
+    // runs before pdl_wait, so that after the previous kernel only the
+    // writes stand between it and the attention kernel.
+    struct Step4 {
+        GroupRec rec;
+        long long grow0;
+        int row0, tot_rows, valid;
+    };
+    int row_carry = 0, full_carry = 0;
+    auto compute4 = [&](int base) {
+        Step4 c;
+        const int gi = base + tid;
+        int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
+        int slots = 0;
+        if (gi < n_groups) {
+            r = grp_req[gi];
+            mt = gi - req_g[r];
+            kvb = grp_kvb[gi];
+            ns = max(1, (kvb - P + split - 1) / split);
+            slots = ns + (P > 0 ? 1 : 0);
+            nv = tile_rows(req_n[r], g, mt);
+        }
+        const int n_rows = (gi < n_groups && slots > 1) ? slots * Hkv * nv : 0;
+        const int full_cnt = gi < n_groups ? (ns - 1) * Hkv : 0;
+        // One scan carries the partial rows (low half) and the full-size
+        // split items (high half); both totals are within int range once the
+        // split length fits the capacities.
+        unsigned long long tot;
+        const unsigned long long ex = block_exclusive_scan<unsigned long long>(
+            ((unsigned long long)full_cnt << 32) | (unsigned)n_rows, &tot, s_ull);
+        c.row0 = row_carry + (int)(ex & 0xffffffffu);
+        c.tot_rows = (int)(tot & 0xffffffffu);
+        const int full0 = s_bucket_base[0] + full_carry + (int)(ex >> 32);
+        full_carry += (int)(tot >> 32);
+        const int tail_b = gi < n_groups ? size_bucket(kvb - P - (ns - 1) * split, split) : -1;
+        // tail items of bucket 0 come after every full-size split
+        const int tail0 = (tail_b > 0 ? s_bucket_base[tail_b] : s_bucket_base[0] + s_full_total) +
+                          warp_claim(tail_b, Hkv, s_bucket_cursor);
+        c.valid = gi < n_groups;
+        c.grow0 = 0;
+        if (c.valid) {
+            const int n = req_n[r], L = req_L[r], q0 = req_q0[r];
+            c.rec.a = make_int4(r, mt, q0, n);
+            c.rec.b = make_int4(L, tile_kv_end(n, L, g, mt), kvb, nv);
+            // arrivals: the splits, plus the prefix tiles over its rows
+            c.grow0 = (long long)q0 * g + (long long)mt * kRowsPerTile;
+            const int arrivals =
+                ns + (P > 0 ? (int)((c.grow0 + nv - 1) / kRowsPerTile - c.grow0 / kRowsPerTile) + 1 : 0);
+            c.rec.c = make_int4(ns, slots > 1 ? c.row0 : -1, slots, arrivals);
+            s_place[tid] = make_int4(full0, tail0, ns, slots);
+        }
+        return c;
+    };
+    // Needs every thread's s_place of this chunk published (a barrier after
+    // compute4).
+    auto write4 = [&](int base, const Step4 &c) {
+        const int gi = base + tid;
+        if (c.valid) {
+            a.group_rec[gi] = c.rec;
+            if (P > 0) {  // the prefix-tile view of this group's rows
+                int4 *m = a.prefix_map + c.grow0;
+                const int nv = c.rec.b.w, slots = c.rec.c.z, arrivals = c.rec.c.w;
+                for (int row = 0; row < nv; ++row) m[row] = make_int4(c.row0 + row, slots * nv, gi, arrivals);
+            }
+        }
+        // Items of this chunk of groups, one (group, kv head) pair per thread.
+        const int chunk_groups = min(kPlanThreads, n_groups - base);
+        for (int p = tid; p < chunk_groups * Hkv; p += kPlanThreads) {
+            const int lg = p / Hkv, h = p - lg * Hkv;
+            const int4 pl = s_place[lg];
+            const int gq = base + lg, ns_g = pl.z;
+            if (pl.w > 1) a.tile_counter[gq * Hkv + h] = 0;
+            for (int s = 0; s < ns_g; ++s) {
+                const long long idx = s < ns_g - 1 ? (long long)pl.x + h * (ns_g - 1) + s : (long long)pl.y + h;
+                if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, grp_req[gq]);
+            }
+        }
+    };
+    const bool early4 = early && n_groups <= kPlanThreads;
+    Step4 c4{};
+    if (early4) {
+        c4 = compute4(0);
+        __syncthreads();
+    }
     if (early) {
         pdl_wait();
         if (tid == 0) {
@@ -444,70 +533,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.header->n_prefix_items =
             P > 0 ? (int)(((long long)a.num_tokens * g + kRowsPerTile - 1) / kRowsPerTile) * Hkv : 0;
     }
-    __syncthreads();
-
-    // 4. partial-row bases (chunked scan over groups) and the decode items.
-    int row_carry = 0, full_carry = 0;
-    for (int base = 0; base < n_groups; base += kPlanThreads) {
-        const int gi = base + tid;
-        int ns = 0, r = 0, mt = 0, kvb = 0, nv = 0;
-        int slots = 0;
-        if (gi < n_groups) {
-            r = grp_req[gi];
-            mt = gi - req_g[r];
-            kvb = grp_kvb[gi];
-            ns = max(1, (kvb - P + split - 1) / split);
-            slots = ns + (P > 0 ? 1 : 0);
-            nv = tile_rows(req_n[r], g, mt);
-        }
-        const int n_rows = (gi < n_groups && slots > 1) ? slots * Hkv * nv : 0;
-        const int full_cnt = gi < n_groups ? (ns - 1) * Hkv : 0;
-        // One scan carries the partial rows (low half) and the full-size
-        // split items (high half); both totals are within int range once the
-        // split length fits the capacities.
-        unsigned long long tot;
-        const unsigned long long ex = block_exclusive_scan<unsigned long long>(
-            ((unsigned long long)full_cnt << 32) | (unsigned)n_rows, &tot, s_ull);
-        const int row0 = row_carry + (int)(ex & 0xffffffffu);
-        const int tot_rows = (int)(tot & 0xffffffffu);
-        const int full0 = s_bucket_base[0] + full_carry + (int)(ex >> 32);
-        full_carry += (int)(tot >> 32);
-        const int tail_b = gi < n_groups ? size_bucket(kvb - P - (ns - 1) * split, split) : -1;
-        // tail items of bucket 0 come after every full-size split
-        const int tail0 = (tail_b > 0 ? s_bucket_base[tail_b] : s_bucket_base[0] + s_full_total) +
-                          warp_claim(tail_b, Hkv, s_bucket_cursor);
-        if (gi < n_groups) {
-            const int n = req_n[r], L = req_L[r], q0 = req_q0[r];
-            GroupRec rec;
-            rec.a = make_int4(r, mt, q0, n);
-            rec.b = make_int4(L, tile_kv_end(n, L, g, mt), kvb, nv);
-            // arrivals: the splits, plus the prefix tiles over its rows
-            const long long grow0 = (long long)q0 * g + (long long)mt * kRowsPerTile;
-            const int arrivals =
-                ns + (P > 0 ? (int)((grow0 + nv - 1) / kRowsPerTile - grow0 / kRowsPerTile) + 1 : 0);
-            rec.c = make_int4(ns, slots > 1 ? row0 : -1, slots, arrivals);
-            a.group_rec[gi] = rec;
-            if (P > 0) {  // the prefix-tile view of this group's rows
-                int4 *m = a.prefix_map + grow0;
-                for (int row = 0; row < nv; ++row) m[row] = make_int4(row0 + row, slots * nv, gi, arrivals);
-            }
-            s_place[tid] = make_int4(full0, tail0, ns, slots);
-        }
+    if (early4) {
+        write4(0, c4);
+        row_carry = c4.tot_rows;
+    } else {
         __syncthreads();
-        // Items of this chunk of groups, one (group, kv head) pair per thread.
-        const int chunk_groups = min(kPlanThreads, n_groups - base);
-        for (int p = tid; p < chunk_groups * Hkv; p += kPlanThreads) {
-            const int lg = p / Hkv, h = p - lg * Hkv;
-            const int4 pl = s_place[lg];
-            const int gq = base + lg, ns_g = pl.z;
-            if (pl.w > 1) a.tile_counter[gq * Hkv + h] = 0;
-            for (int s = 0; s < ns_g; ++s) {
-                const long long idx = s < ns_g - 1 ? (long long)pl.x + h * (ns_g - 1) + s : (long long)pl.y + h;
-                if (idx < a.items_cap) a.items[idx].v = make_int4(gq, h, s, grp_req[gq]);
-            }
+        for (int base = 0; base < n_groups; base += kPlanThreads) {
+            const Step4 c = compute4(base);
+            __syncthreads();
+            write4(base, c);
+            __syncthreads();
+            row_carry += c.tot_rows;
         }
-        __syncthreads();
-        row_carry += tot_rows;
     }
     if (tid == 0) a.header->n_partial_rows = row_carry;
 
