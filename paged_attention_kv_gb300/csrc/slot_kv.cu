@@ -82,17 +82,37 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__rest
                                 uint4 *__restrict__ kv_cache, long long num_slots, int num_kv_heads,
                                 int chunks_per_row, int32_t *status, const SlotSource src_tables) {
     pdl_launch_dependents();
-    pdl_wait();
-    if (kFused && blockIdx.x == 0 && threadIdx.x == 0 &&
-        (__ldg(src_tables.qsl) != 0 || __ldg(src_tables.qsl + src_tables.num_reqs) != num_tokens))
-        raise_status(status, PKV_DEV_BAD_QSL);
     constexpr int C = 4 / R;  // chunks per lane per row and pass
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const int per_kv = num_kv_heads * chunks_per_row;  // 16-byte chunks of one token's K (or V) row
     const long long tile = (long long)PKV_BLOCK_SIZE * chunks_per_row;  // chunks of one (block, K|V, head) tile
     const long long units = 2 * num_tokens;
-    for (long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g * R < units; g += nwarps) {
+    const long long g0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // Fused: the tables hold this call's values when it is enqueued, so the
+    // slots of the warp's first pass (every pass, for any grid this library
+    // launches) are resolved before waiting on the previous kernel; that
+    // kernel (in a step, the previous attention) then no longer waits on the
+    // lookups. Nothing is written before the wait: bad metadata is reported
+    // after it, by resolving the slot again with the status word.
+    int32_t first_slot[R];
+    bool qsl_bad = false;
+    if (kFused) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const long long u = g0 * R + j;
+            int32_t s0 = -1;
+            if (u < units && lane == 0)
+                s0 = token_slot(src_tables.block_table, src_tables.num_reqs, src_tables.max_blocks_per_req,
+                                src_tables.seq_lens, src_tables.qsl, src_tables.num_blocks, (int)(u >> 1), nullptr);
+            first_slot[j] = __shfl_sync(0xffffffffu, s0, 0);
+        }
+        qsl_bad = blockIdx.x == 0 && threadIdx.x == 0 &&
+                  (__ldg(src_tables.qsl) != 0 || __ldg(src_tables.qsl + src_tables.num_reqs) != num_tokens);
+    }
+    pdl_wait();
+    if (qsl_bad) raise_status(status, PKV_DEV_BAD_QSL);
+    for (long long g = g0; g * R < units; g += nwarps) {
         const uint4 *src[R];
         uint4 *dst[R];
 #pragma unroll
@@ -106,13 +126,16 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__rest
             int32_t slot;
             if (kFused) {
                 // lane 0 resolves the slot (reporting bad metadata once, on the
-                // token's K row) and stores it; the warp shares it
+                // token's K row) and stores it; the warp shares it. The first
+                // pass has it already; a failed lookup is redone here to
+                // report it.
                 int32_t s0 = 0;
-                if (lane == 0)
+                const bool have = g == g0;
+                if (lane == 0 && (!have || first_slot[j] < 0))
                     s0 = token_slot(src_tables.block_table, src_tables.num_reqs, src_tables.max_blocks_per_req,
                                     src_tables.seq_lens, src_tables.qsl, src_tables.num_blocks, (int)t,
                                     kv == 0 ? status : nullptr);
-                slot = __shfl_sync(0xffffffffu, s0, 0);
+                slot = have && first_slot[j] >= 0 ? first_slot[j] : __shfl_sync(0xffffffffu, s0, 0);
                 if (lane == 0 && kv == 0) src_tables.slot_out[t] = slot;
             } else {
                 slot = __ldg(slot_mapping + t);
