@@ -135,6 +135,13 @@ int paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, in
  * slot_mapping (device int32 [num_tokens], written) and used for that
  * token's K/V at once. Same results as the two calls in sequence; one kernel
  * launch fewer per step. Arguments as for those two calls.
+ *
+ * Ordering: block_table, seq_lens and query_start_loc must hold this call's
+ * values when the call is enqueued (written by host copies, or by kernels
+ * that complete before their dependents launch): the slots are looked up
+ * while the stream's previous kernel may still be running. k, v and the
+ * pool are read, and slot_mapping, status and the pool written, only after
+ * every earlier kernel on the stream has completed.
  */
 int paged_kv_write_slots(const void *k, const void *v, const int32_t *block_table, int32_t num_reqs,
                          int32_t max_blocks_per_req, const int32_t *seq_lens, const int32_t *query_start_loc,
