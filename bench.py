@@ -11,9 +11,16 @@ workload is the Llama-3-8B-shaped decode batch (32 q / 8 kv heads, head 128,
 Prints one JSON line. ``value`` is query tokens per second for the whole job
 (all ranks) with inputs resident in HBM; ``e2e`` is the same metric with
 each step's inputs copied from pinned host memory and the output copied back
-inside the timed region. ``roofline`` covers the attention kernel, timed
-live with CUDA events on its stream; ``cpu_baseline`` is the fp64 oracle on
-the host cores over a bounded sample of the same workload.
+inside the timed region (the median of several timed runs of the K steps).
+``roofline`` covers the attention kernel, timed live with CUDA events on its
+stream; ``cpu_baseline`` is the fp64 oracle on the host cores over a bounded
+sample of the same workload, with a one-thread figure beside it.
+
+After the headline (Llama-3-8B decode) workload the same run times the
+prefix-sharing batch and the mixed chunked-prefill + decode batch the same
+way and reports them under ``gates``, each with its own roofline(s), per-step
+spread and clocks. Clocks are read through NVML every millisecond from a
+background thread while the GPU works.
 
 ``--impl reference`` times the oracle itself (the reference arm of this
 comparison) on the same workload and prints the same line shape.
@@ -71,6 +78,10 @@ def parse_args():
                         "per model layer, as a real step over a model's layers does) until their total exceeds "
                         "512 MiB; flush: write and read 512 MiB before every step and time steps one by one; "
                         "auto: layers when one pool is under 512 MiB, else none (the step's reads are GBs)")
+    p.add_argument("--gates", default="auto",
+                   help="other workloads timed in the same run after the headline one, comma-separated; "
+                        "auto: prefix and mixed (the prefix-sharing and mixed batches) when the headline "
+                        "workload is llama8b; none: only the headline workload")
     p.add_argument("--op", choices=("step", "kv_transfer", "kv_write"), default="step",
                    help="kv_transfer: time block gather + scatter of the workload's context blocks; "
                         "kv_write: time the KV write alone, on the workload's new tokens and on a "
@@ -259,12 +270,76 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> fl
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# NVML clock-event reason bits that the line reports by name.
+NVML_REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+                (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
 
 
-class ClockSampler:
+class NvmlClockSampler:
+    """SM clock, power, utilisation and clock-event reasons of one GPU,
+    read through NVML (read-only queries of libnvidia-ml) every `interval_s`
+    from a background thread, so that even a timed region of a few
+    milliseconds holds several samples. Each sample is (wall time, SM MHz,
+    max SM MHz, watts, reason bits, GPU utilisation %)."""
+
+    def __init__(self, torch_device_index: int, interval_s: float = 0.001):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if not self._handle_by_uuid(torch_device_index) and \
+                self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch_device_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.rows = []
+        self.interval = interval_s
+        self._stop = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _handle_by_uuid(self, idx: int) -> bool:
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(idx).uuid)
+        except Exception:
+            return False
+        name = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        return self.lib.nvmlDeviceGetHandleByUUID(name.encode(), self.ct.byref(self.h)) == 0
+
+    def _run(self):
+        ct, lib, h = self.ct, self.lib, self.h
+
+        class Util(ct.Structure):
+            _fields_ = [("gpu", ct.c_uint), ("memory", ct.c_uint)]
+        clk, pw, rs, ut = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0), Util()
+        while not self._stop.is_set():
+            t = time.time()
+            lib.nvmlDeviceGetClockInfo(h, ct.c_int(1), ct.byref(clk))
+            lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw))
+            self.reasons_fn(h, ct.byref(rs))
+            lib.nvmlDeviceGetUtilizationRates(h, ct.byref(ut))
+            self.rows.append((t, float(clk.value), self.max_mhz, pw.value / 1000.0, int(rs.value), int(ut.gpu)))
+            self._stop.wait(self.interval)
+
+    def stop(self):
+        self._stop.set()
+        self.thread.join(timeout=5)
+
+
+class SmiClockSampler:
+    """The same samples from `nvidia-smi --query-gpu ... -lms 20` (used when
+    NVML cannot be loaded)."""
+
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.lines = []
+        self.rows = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-i",
@@ -281,30 +356,50 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        self.lines = [ln for ln in out.splitlines() if ln.strip()]
-
-    def summary(self, t0: float, t1: float) -> dict:
-        rows = []
-        for ln in self.lines:
+        bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20, "sw_power_cap": 0x4}
+        for ln in out.splitlines():
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 10:
                 continue
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+                rb = 0
+                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                   parts[6:10]):
+                    if v.lower() == "active":
+                        rb |= bits[name]
+                self.rows.append((ts + frac, float(parts[2]), float(parts[3]), float(parts[4] or 0), rb, 100))
             except (ValueError, IndexError):
                 continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        window = "timed"
-        if len(inside) < 3:
-            inside, window = rows, "warmup+timed"
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def start_clock_sampler(local_rank: int):
+    try:
+        return NvmlClockSampler(local_rank)
+    except (OSError, AttributeError):
+        return SmiClockSampler(local_rank)
+
+
+def clock_summary(rows, window, busy, ms_per_step=None) -> dict:
+    """Clocks over the timed window (t0, t1); when it holds fewer than three
+    samples, over the workload's busy window (its timed, per-kernel and
+    per-step passes back to back), and failing that over every sample."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+    window = "timed"
+    if len(inside) < 3:
+        inside, window = [r for r in rows if busy[0] <= r[0] <= busy[1]], "this workload's timed and per-kernel passes"
+    if len(inside) < 3:
+        inside, window = rows, "all samples from warm-up to the last pass"
+    reasons = sorted({name for r in inside for bit, name in NVML_REASONS if r[4] & bit})
+    mhz = float(np.median([r[1] for r in inside]))
+    out = {"sm_mhz": mhz, "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons, "samples": len(inside),
+           "window": window, "power_w_max": max(r[3] for r in inside)}
+    if ms_per_step is not None:
+        out["step_kcycles_at_median_mhz"] = ms_per_step * 1e-3 * mhz * 1e6 / 1e3
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -338,13 +433,14 @@ def host_copy(ten):
     return {k: wl.bf16_bits(v).copy() for k, v in ten.items()}
 
 
-def cpu_baseline(batch, host, target_s=10.0, cap_s=30.0) -> dict:
+def cpu_baseline(batch, host, target_s=10.0, cap_s=30.0, single_s=3.0) -> dict:
     """The oracle as it stands on every host core, over whole requests of
-    the workload, repeated until about target_s of work."""
+    the workload, repeated until about target_s of work; then the same on one
+    thread for about single_s."""
     threads = os.cpu_count() or 1
     order = np.arange(batch.num_reqs)
     t0 = time.perf_counter()
-    tokens = oracle_step(batch, host, order[:4], threads)
+    oracle_step(batch, host, order[:4], threads)
     per_req = (time.perf_counter() - t0) / 4
     n = int(min(batch.num_reqs, max(4, target_s / max(per_req, 1e-6))))
     done, reqs_done, start = 0, 0, time.perf_counter()
@@ -355,9 +451,19 @@ def cpu_baseline(batch, host, target_s=10.0, cap_s=30.0) -> dict:
         reqs_done += n
         i += n
     el = time.perf_counter() - start
+    # one thread, whole requests, bounded to about single_s
+    done1, reqs1, i, start1 = 0, 0, 0, time.perf_counter()
+    while time.perf_counter() - start1 < single_s:
+        sel = order[(np.arange(1) + i) % batch.num_reqs]
+        done1 += oracle_step(batch, host, sel, 1)
+        reqs1 += 1
+        i += 1
+    el1 = time.perf_counter() - start1
     return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{reqs_done} requests of the {batch.workload} workload ({done} query tokens, whole "
-                      f"step: slot mapping + KV write + attention), fp64, {el:.1f} s"}
+                      f"step: slot mapping + KV write + attention), fp64, {el:.1f} s",
+            "single_thread": {"value": done1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{reqs1} requests one at a time ({done1} query tokens), fp64, {el1:.1f} s"}}
 
 
 def run_reference(args, batch, rank):
@@ -399,6 +505,176 @@ def run_reference(args, batch, rank):
 # our arm
 # --------------------------------------------------------------------------
 
+GATE_WORKLOADS = ("prefix", "mixed")
+
+
+def device_pass(args, batch, ten, pkv, torch, dev, dist, graph=False):
+    """One workload with inputs resident in HBM: W warm-up steps, the K
+    timed steps back to back (the headline), the same K steps with events
+    between the attention launches (per-kernel times) and K steps each
+    between two events (the per-step spread)."""
+    mode, layers = l2_mode(args, batch)
+    bufs = [pkv.StepBuffers(batch, ten)]
+    for _ in range(layers - 1):  # one pool per layer; the step's other inputs are shared
+        bufs.append(pkv.StepBuffers(batch, {**ten, "kv_cache": ten["kv_cache"].clone()}))
+    graphs = [pkv.StepGraph(b) for b in bufs] if graph else None
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    prepared = [b.prepared() for b in bufs]  # the headline pass enqueues each step through prebuilt C arguments
+
+    def step(i, timed_kernels=False):
+        b = bufs[i % layers]
+        if graphs is not None and not timed_kernels:
+            graphs[i % layers].replay()
+            return
+        if not timed_kernels:
+            prepared[i % layers]()
+            return
+        pkv.paged_slot_mapping(b.block_table, b.seq_lens, b.query_start_loc, b.num_tokens,
+                               batch.num_blocks, b.slot_mapping, b.status)
+        pkv.paged_kv_write(b.k, b.v, b.slot_mapping, b.kv_cache, b.status)
+        pkv.paged_attention(b.q, b.kv_cache, b.block_table, b.seq_lens, b.query_start_loc, batch.scale,
+                            b.out, b.workspace, events=ev[i], max_query_len=b.max_query_len)
+
+    scrub = torch.empty(L2_SCRUB_BYTES, dtype=torch.uint8, device=dev) if mode == "flush" else None
+    for i in range(max(args.warmup, layers)):
+        step(i)
+    per_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for e4 in ev:  # create the event handles outside the timed region
+        for e in e4:
+            e.record(stream)
+    for a, b in per_step:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    if scrub is not None:
+        # cold L2 every step: scrub, then time the step alone
+        for i in range(args.steps):
+            scrub_l2(scrub)
+            per_step[i][0].record(stream)
+            step(i)
+            per_step[i][1].record(stream)
+        torch.cuda.synchronize()
+        step_ms = [x.elapsed_time(y) for x, y in per_step]
+        elapsed_ms = float(sum(step_ms))
+    else:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = t_start.elapsed_time(t_end)
+    wall1 = time.time()
+    # Per-kernel pass: the same K steps with events between the attention
+    # launches (an event between two launches stops the next one from
+    # starting early, so the headline pass above runs without them).
+    for i in range(args.steps):
+        if scrub is not None:
+            scrub_l2(scrub)
+        step(i, timed_kernels=True)
+    torch.cuda.synchronize()
+    if scrub is None:
+        # Per-step pass: each step between two events (which also stop
+        # consecutive steps from overlapping), for the spread of step times.
+        for i in range(args.steps):
+            per_step[i][0].record(stream)
+            step(i)
+            per_step[i][1].record(stream)
+        torch.cuda.synchronize()
+        step_ms = [x.elapsed_time(y) for x, y in per_step]
+    wall2 = time.time()
+    if dist:
+        dist.barrier()
+    for b in bufs:
+        st = pkv.pkv_read_status(b.status)
+        wst = pkv.pkv_read_status(b.workspace)
+        if st or wst:
+            raise RuntimeError(f"device status bits set ({batch.workload}): {st:#x} {wst:#x}")
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+    return {"elapsed_ms": elapsed_ms, "mode": mode, "layers": layers, "bufs": bufs, "scrub": scrub,
+            "plan_ms": float(np.mean([e4[0].elapsed_time(e4[1]) for e4 in ev])),
+            "chunk_ms": float(np.mean([e4[1].elapsed_time(e4[2]) for e4 in ev])),
+            "attn_ms": [e4[2].elapsed_time(e4[3]) for e4 in ev],
+            "attn_call_ms": [e4[0].elapsed_time(e4[3]) for e4 in ev],
+            "step_ms": step_ms, "window": (wall0, wall1), "busy": (wall0, wall2),
+            "graph": graphs is not None}
+
+
+def spread(ms: list) -> dict:
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median_ms": float(np.median(a)), "min_ms": float(a.min()), "max_ms": float(a.max()),
+            "mean_ms": float(a.mean()), "n": int(a.size)}
+
+
+def device_fields(batch, res, world, steps, peaks) -> dict:
+    """The bench line's device-resident fields of one workload: the headline
+    rate, the split-KV kernel's HBM roofline (bytes counted once per
+    physical block: a shared prefix counts once), the chunk-tile kernel's
+    tensor roofline when the batch has chunk tiles, per-kernel times and the
+    per-step spread."""
+    chunk_mask = chunk_requests(batch)
+    ab = algorithmic_bytes(batch, only=~chunk_mask)  # what the split-KV kernel reads and writes
+    ab_all = algorithmic_bytes(batch)
+    kernel_ms = float(np.mean(res["attn_ms"]))
+    achieved = ab["attention_total"] / (kernel_ms * 1e-3) / 1e9
+    ms_per_step = res["elapsed_ms"] / steps
+    per_step = spread(res["step_ms"])
+    per_step["how"] = ("each step between two CUDA events (no overlap with its neighbours)" if res["mode"] != "flush"
+                       else "each step alone after an L2 flush")
+    return {
+        "value": job_tokens_per_s(world, batch.num_tokens, ms_per_step),
+        "ms_per_step": ms_per_step,
+        "roofline": {"bound": "hbm", "kernel": "attention decode_kernel (split-KV)", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     # the committed capture is of the Llama-3-8B batch: other batches get none
+                     "traffic": profiled_traffic() if batch.workload == "llama8b" else None,
+                     "algorithmic_bytes_per_launch": ab["attention_total"],
+                     "kernel_us": kernel_ms * 1e3,
+                     "kernel_us_spread": {k[:-3] + "_us": v * 1e3 for k, v in spread(res["attn_ms"]).items()
+                                          if k.endswith("_ms")},
+                     "attention_call_us": float(np.mean(res["attn_call_ms"])) * 1e3,
+                     "frac_of_8tbps_nominal": achieved / 8000.0},
+        "kernels_us": {"work_list": res["plan_ms"] * 1e3, "chunk_tiles": res["chunk_ms"] * 1e3,
+                       "split_kv": kernel_ms * 1e3},
+        "roofline_chunk_tiles": chunk_roofline(batch, res["chunk_ms"], peaks) if chunk_mask.any() else None,
+        "step_spread": per_step,
+        "kv_bytes_per_step": {"unique": ab_all["kv"], "logical": ab_all["logical_kv"]},
+    }
+
+
+def run_gates(args, pkv, torch, wl, dev, dist, rank, world, peaks):
+    """The other two configurations the bandwidth target is read on, timed
+    the same way in the same run: the prefix-sharing batch (its fraction is
+    on unique bytes: the 64 shared blocks count once) and the mixed batch
+    (chunk tiles beside split-KV decode: two rooflines)."""
+    if args.gates == "auto":
+        names = GATE_WORKLOADS if args.workload == "llama8b" else ()
+    else:
+        names = tuple(x for x in args.gates.split(",") if x)
+    out = {}
+    for name in names:
+        if name == args.workload or name == "none":
+            continue
+        batch = rank_batch(name, rank)
+        ten = wl.make_tensors(batch, device=dev)
+        res = device_pass(args, batch, ten, pkv, torch, dev, dist)
+        f = device_fields(batch, res, world, args.steps, peaks)
+        f["config"] = workload_config(batch, l2_note(batch, res["mode"], res["layers"]))
+        f["clocks"] = (res["window"], res["busy"])  # replaced by the summary once the sampler has stopped
+        f["gpu_launches"] = launches_per_step(batch) * args.steps
+        out[name] = f
+        del res, ten
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -430,96 +706,20 @@ def main():
         run_kv_write(args, batch, ten, pkv, torch, dev, dist, rank, world)
         return
     host = host_copy(ten) if (rank == 0 and world == 1 and not args.skip_cpu_baseline) else None
-    mode, layers = l2_mode(args, batch)
-    bufs = [pkv.StepBuffers(batch, ten)]
-    for _ in range(layers - 1):  # one pool per layer; the step's other inputs are shared
-        bufs.append(pkv.StepBuffers(batch, {**ten, "kv_cache": ten["kv_cache"].clone()}))
-    buf = bufs[0]
-    graphs = [pkv.StepGraph(b) for b in bufs] if args.graph else None
-    stream = torch.cuda.current_stream()
-
-    nev = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nev)]
-
-    # the headline pass enqueues each step through prebuilt C arguments
-    prepared = [b.prepared() for b in bufs]
-
-    def step(i, timed_kernels=False):
-        b = bufs[i % layers]
-        if graphs is not None and not timed_kernels:
-            graphs[i % layers].replay()
-            return
-        if not timed_kernels:
-            prepared[i % layers]()
-            return
-        pkv.paged_slot_mapping(b.block_table, b.seq_lens, b.query_start_loc, b.num_tokens,
-                               batch.num_blocks, b.slot_mapping, b.status)
-        pkv.paged_kv_write(b.k, b.v, b.slot_mapping, b.kv_cache, b.status)
-        pkv.paged_attention(b.q, b.kv_cache, b.block_table, b.seq_lens, b.query_start_loc, batch.scale,
-                            b.out, b.workspace, events=ev[i] if timed_kernels else None,
-                            max_query_len=b.max_query_len)
-
-    scrub = torch.empty(L2_SCRUB_BYTES, dtype=torch.uint8, device=dev) if mode == "flush" else None
-    sampler = ClockSampler(local_rank)
-    for i in range(max(args.warmup, layers)):
-        step(i)
-    # create the event handles outside the timed region
-    for e4 in ev:
-        for e in e4:
-            e.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    wall0 = time.time()
-    if scrub is not None:
-        # cold L2 every step: scrub, then time the step alone
-        ts = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.steps):
-            scrub_l2(scrub)
-            ts[i][0].record(stream)
-            step(i)
-            ts[i][1].record(stream)
-        torch.cuda.synchronize()
-        elapsed_ms = float(sum(a.elapsed_time(b) for a, b in ts))
-    else:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(i)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        elapsed_ms = t_start.elapsed_time(t_end)
-    wall1 = time.time()
-    # Per-kernel pass: the same K steps with events between the attention
-    # launches (an event between two launches stops the next one from
-    # starting early, so the headline pass above runs without them).
-    for i in range(args.steps):
-        if scrub is not None:
-            scrub_l2(scrub)
-        step(i, timed_kernels=True)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    sampler.stop()
-    for b in bufs:
-        st = pkv.pkv_read_status(b.status)
-        wst = pkv.pkv_read_status(b.workspace)
-        if st or wst:
-            raise RuntimeError(f"device status bits set: {st:#x} {wst:#x}")
-    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
-
-    plan_ms = float(np.mean([e4[0].elapsed_time(e4[1]) for e4 in ev]))
-    chunk_ms = float(np.mean([e4[1].elapsed_time(e4[2]) for e4 in ev]))
-    attn_ms = [e4[2].elapsed_time(e4[3]) for e4 in ev]
-    attn_call_ms = [e4[0].elapsed_time(e4[3]) for e4 in ev]
-    kernel_ms = float(np.mean(attn_ms))
+    peaks = measured_peaks()
+    sampler = start_clock_sampler(local_rank)
+    res = device_pass(args, batch, ten, pkv, torch, dev, dist, graph=args.graph)
 
     # end to end: inputs from pinned host memory, output back, every step
     e2e = None
     if not args.skip_e2e:
-        e2e = run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub)
+        e2e = run_e2e(args, batch, ten, res["bufs"], pkv, torch, dev, dist, res["scrub"])
+
+    gates = {}
+    if args.op == "step" and args.gates != "none":
+        del res["bufs"]
+        gates = run_gates(args, pkv, torch, wl, dev, dist, rank, world, peaks)
+    sampler.stop()
 
     cpu = None
     if host is not None:
@@ -530,36 +730,29 @@ def main():
             dist.destroy_process_group()
         return
 
-    chunk_mask = chunk_requests(batch)
-    ab = algorithmic_bytes(batch, only=~chunk_mask)   # what the split-KV kernel reads and writes
-    ab_all = algorithmic_bytes(batch)
-    peaks = measured_peaks()
-    achieved = ab["attention_total"] / (kernel_ms * 1e-3) / 1e9
-    ms_per_step = elapsed_ms / args.steps
-    value = job_tokens_per_s(world, batch.num_tokens, ms_per_step)
-    clocks = sampler.summary(wall0, wall1)
+    fields = device_fields(batch, res, world, args.steps, peaks)
+    clocks = clock_summary(sampler.rows, res["window"], res["busy"], fields["ms_per_step"])
+    for g in gates.values():
+        g["clocks"] = clock_summary(sampler.rows, *g["clocks"], g["ms_per_step"])
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": fields["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": fields["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block tables)",
-        "config": {**workload_config(batch, l2_note(batch, mode, layers)), "parallelism": f"{world} independent replicas" if world > 1
-                   else "single GPU", "launch": "CUDA graph replay" if graphs is not None else "eager, PDL launches"},
-        "roofline": {"bound": "hbm", "kernel": "attention decode_kernel (split-KV)", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     # the committed capture is of the Llama-3-8B batch: other batches get none
-                     "traffic": profiled_traffic() if batch.workload == "llama8b" else None,
-                     "algorithmic_bytes_per_launch": ab["attention_total"],
-                     "kernel_us": kernel_ms * 1e3, "attention_call_us": float(np.mean(attn_call_ms)) * 1e3,
-                     "frac_of_8tbps_nominal": achieved / 8000.0},
-        "kernels_us": {"work_list": plan_ms * 1e3, "chunk_tiles": chunk_ms * 1e3, "split_kv": kernel_ms * 1e3},
-        "roofline_chunk_tiles": chunk_roofline(batch, chunk_ms, peaks) if chunk_mask.any() else None,
+        "config": {**workload_config(batch, l2_note(batch, res["mode"], res["layers"])),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+                   "launch": "CUDA graph replay" if res["graph"] else "eager, PDL launches"},
+        "roofline": fields["roofline"],
+        "kernels_us": fields["kernels_us"],
+        "roofline_chunk_tiles": fields["roofline_chunk_tiles"],
+        "step_spread": fields["step_spread"],
         "gpu_launches": launches_per_step(batch) * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "kv_bytes_per_step": {"unique": ab_all["kv"], "logical": ab_all["logical_kv"]},
+        "kv_bytes_per_step": fields["kv_bytes_per_step"],
     }
+    if gates:
+        line["gates"] = gates
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -683,6 +876,9 @@ def run_kv_write(args, batch, ten, pkv, torch, dev, dist, rank, world):
         "gpu_launches": 2 * args.steps}), flush=True)
 
 
+E2E_REPS = 5
+
+
 def run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub=None):
     """K steps through the library's host-buffer pipeline
     (``binding.HostStepPipeline``): every step copies its inputs (q, k, v
@@ -692,7 +888,12 @@ def run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub=None):
     The pool stays resident: it is the layer's KV state, not a per-step
     input; with several pools (``bufs``, one per layer) consecutive steps
     rotate over them as in the device-resident pass. With ``scrub`` every
-    step runs alone after an L2 flush, copies included."""
+    step runs alone after an L2 flush, copies included.
+
+    The K steps are timed E2E_REPS times; ``value`` is the median repetition
+    (every step of this loop waits on the host for its input slot, so a
+    stall of the host thread lands in the timed region; the repetitions
+    show whether one did)."""
     buf = bufs[0]
     layers = len(bufs)
     s = batch.shape
@@ -715,28 +916,31 @@ def run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub=None):
     for i in range(max(3, args.warmup)):
         submit(i)
     pipe.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    if scrub is not None:
-        ms = 0.0
-        for i in range(args.steps):
-            scrub_l2(scrub)
-            torch.cuda.synchronize()
+    reps = []
+    for _ in range(E2E_REPS):
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if scrub is not None:
+            ms = 0.0
+            for i in range(args.steps):
+                scrub_l2(scrub)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(pipe.h2d)
+                submit(i)
+                b.record(pipe.d2h)
+                pipe.synchronize()
+                ms += a.elapsed_time(b)
+        else:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(pipe.h2d)
-            submit(i)
+            for i in range(args.steps):
+                submit(i)
             b.record(pipe.d2h)
             pipe.synchronize()
-            ms += a.elapsed_time(b)
-    else:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(pipe.h2d)
-        for i in range(args.steps):
-            submit(i)
-        b.record(pipe.d2h)
-        pipe.synchronize()
-        ms = a.elapsed_time(b)
+            ms = a.elapsed_time(b)
+        reps.append(max_over_ranks(ms, dist, dev) / args.steps)
     st, wst = pipe.read_status()
     if st or wst:
         raise RuntimeError(f"device status bits set in the host-buffer steps: {st:#x} {wst:#x}")
@@ -744,10 +948,12 @@ def run_e2e(args, batch, ten, bufs, pkv, torch, dev, dist, scrub=None):
     last = args.steps - 1
     if not torch.equal(outs[last % 2].view(torch.int16), bufs[last % layers].out.cpu().view(torch.int16)):
         raise RuntimeError("host-buffer step output differs from the device step")
-    ms = max_over_ranks(ms, dist, dev)
+    ms_step = float(np.median(reps))
     world = dist.get_world_size() if dist else 1
-    return {"value": job_tokens_per_s(world, batch.num_tokens, ms / args.steps), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+    return {"value": job_tokens_per_s(world, batch.num_tokens, ms_step), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_step,
+            "reps_ms_per_step": reps,
+            "how": f"median of {E2E_REPS} timed runs of the same {args.steps} steps",
             "path": "binding.HostStepPipeline: one packed pinned-host-to-device copy of the step's inputs and one "
                     "device-to-host copy of its output per step, overlapped with the neighbouring steps' kernels"}
 

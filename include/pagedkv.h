@@ -288,6 +288,13 @@ int paged_attention_bounded(const void *q, int32_t num_tokens, int32_t num_q_hea
  * stays inside the array and cannot be read back; bad metadata is still
  * skipped safely. Arguments, layouts and results are otherwise those of
  * paged_attention.
+ *
+ * Lifetime: the array's device address and the kernels' attributes are
+ * looked up once per device and kept for the life of the process. The
+ * library does not survive cudaDeviceReset (or any other teardown of a
+ * device's primary context): after one, the cached address may name memory
+ * of the old context, so no entry point of this library may be called again
+ * in that process.
  */
 int paged_attention_static(const void *q, int32_t num_tokens, int32_t num_q_heads,
                            const void *kv_cache, const pkv_cache_desc *desc,

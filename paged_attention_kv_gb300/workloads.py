@@ -125,7 +125,10 @@ def _tables(rng, blocks_per_req, shared_blocks, pool_factor=1.25, num_blocks=Non
 
 
 def make_batch(workload: str, seed_offset: int = 0) -> Batch:
-    """The named workload, drawn from seed ``BASE_SEED + index + seed_offset``."""
+    """The named workload. Its lengths and block tables are drawn with numpy's
+    PCG64 generator from seed ``BASE_SEED + n + seed_offset``, where n is the
+    workload's 1-based position in ``WORKLOADS`` (the configuration number:
+    tiny 1, tinyllama 2, llama8b 3, mixed 4, prefix 5, specdec 6)."""
     idx = WORKLOADS.index(workload)
     seed = BASE_SEED + idx + 1 + seed_offset
     rng = np.random.Generator(np.random.PCG64(seed))
