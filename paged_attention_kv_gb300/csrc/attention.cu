@@ -612,7 +612,7 @@ struct DecodeArgs {
     float2 *part_ml;
     float *part_o;
     int beside_chunk;  // launched after the chunk kernel, running beside it (see attention_impl)
-    int static_first;  // CTA b starts on item b (the batch's rows promise at least one item per CTA)
+    int static_first;  // CTA b starts on item b (not beside the chunk kernel)
 };
 
 // Per-item description handed from the producer to the consumers through
@@ -1226,12 +1226,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
         if (lane == 0) tma_prefetch_desc(&kv_map);
         uint32_t e = 0;  // ring element counter
         bool ok = true;
-        // When the batch has about one item per CTA or more, CTA b starts on
-        // item b (the list is longest first, so the longest items spread
-        // over the SMs) and later items come from the counter, past the
-        // grid's first items (a CTA whose b is past the list just leaves).
-        // Otherwise, and beside the chunk kernel (where some CTAs start only
-        // when chunk CTAs leave), every item is claimed from the counter.
+        // CTA b starts on item b (the list is longest first, so the longest
+        // items spread over the SMs) and later items come from the counter,
+        // past the grid's first items (a CTA whose b is past the list just
+        // leaves). Beside the chunk kernel (where some CTAs start only when
+        // chunk CTAs leave), every item is claimed from the counter.
         const int claim_base = a.static_first ? (int)gridDim.x : 0;
         int cur = (int)blockIdx.x;
         if (!a.static_first) {
@@ -1687,12 +1686,12 @@ int attention_impl(const void *q, int32_t num_tokens, int32_t num_q_heads, const
         ca.beside = 1;
         da.beside_chunk = 1;
     }
-    // Every 16 rows of a kv head make at least one split-KV item, so this
-    // many rows promise an item per CTA (rows the chunk kernel takes count
-    // too: a wrong guess only leaves some CTAs idle at first, never a wrong
-    // result). Deciding on the host spares the CTAs a dependent read of the
-    // work list's item count before their first claim.
-    da.static_first = !da.beside_chunk && ((long long)num_tokens * da.group / kRowsPerTile) * Hkv >= ctas ? 1 : 0;
+    // CTA b starts on item b without a claim (a CTA whose b is past the
+    // list leaves, as it would after a claim past it): one atomic round
+    // trip less before the first copies, which is most of a small batch's
+    // start-up. Beside the chunk kernel some CTAs start only when chunk
+    // CTAs leave, so there every item is claimed from the counter.
+    da.static_first = !da.beside_chunk ? 1 : 0;
     if (chunk_ok && chunk_launch(D, di->sm_count, kv_map_chunk, q_map, ca, st) != cudaSuccess) return PKV_E_CUDA;
     record(events, 2, st);
     err = launch_decode();
