@@ -30,11 +30,12 @@
 // to be consumed; the tensor core runs PV(x-1) and S(x+1) meanwhile. One
 // warp per row would leave each SM sub-partition a single long dependency
 // chain per tile; four shorter ones interleave. Warps: 0-15 softmax and
-// output (warp w: lane quadrant w % 4, key part w / 4), 16 TMA producer (Q
-// tile; K and V tiles of 8 blocks; K runs a tile ahead of V), 17 MMA issuer
-// (one elected lane) and TMEM owner. Every wait is bounded; on a timeout the
-// CTA raises PKV_DEV_TIMEOUT, stops, lets its in-flight copies and MMAs
-// finish and frees its TMEM.
+// output (warp w: lane quadrant w % 4, key part w / 4), 16 copies (item
+// claims, Q tile, K tiles of 8 blocks), 17 MMA issuer (one elected lane) and
+// TMEM owner, 18 copies of the V tiles (two warps issuing bulk copies get
+// more into one SM than one warp issuing them all). Every wait is bounded;
+// on a timeout the CTA raises PKV_DEV_TIMEOUT, stops, lets its in-flight
+// copies and MMAs finish and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,8 +54,10 @@ namespace {
 constexpr int kParts = 4;                          // softmax warps per TMEM lane quadrant
 constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kPartKeys = kChunkKeys / kParts;     // keys of one warp's part
-constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kChunkThreads = 32 * (kSoftmaxWarps + 2);
+// Two copy warps, one for K and one for V: one SM takes in more when two
+// warps issue its bulk copies than when one issues them all.
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1, kVWarp = kSoftmaxWarps + 2;
+constexpr int kChunkThreads = 32 * (kSoftmaxWarps + 3);
 // TMEM columns: S0 | S1 (fp32, 128 each) | P0 | P1 (bf16 pairs, 64 each) | O (D).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 256, kColO = 384;
@@ -78,7 +81,8 @@ struct ChunkBars {
     static constexpr int kOFree = kODone + 1;
     static constexpr int kDrain = kOFree + 1;
     static constexpr int kXBar = kDrain + 1;      // [4 quadrants][2 parities]
-    static constexpr int kCount = kXBar + 8;
+    static constexpr int kDFull = kXBar + 8;      // the item is in desc (for the V copy warp)
+    static constexpr int kCount = kDFull + 1;
 };
 
 // Item as the producer hands it to the other roles.
@@ -133,6 +137,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     uint64_t *s_full = bar + B::kSFull, *p_full = bar + B::kPFull, *pv_done = bar + B::kPvDone;
     uint64_t *o_done = bar + B::kODone, *o_free = bar + B::kOFree, *drain = bar + B::kDrain;
     uint64_t *xbar = bar + B::kXBar;
+    uint64_t *d_full = bar + B::kDFull;
     float *xbuf = reinterpret_cast<float *>(smem + S::kOffX);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kOffTmem);
     ChunkDesc *desc = reinterpret_cast<ChunkDesc *>(smem + S::kOffDesc);
@@ -145,7 +150,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     if (threadIdx.x == 0) {
         s_abort = 0;
         mbar_init(q_full, 1);
-        mbar_init(q_taken, 1 + kSoftmaxWarps);  // the MMA warp and the softmax warps
+        mbar_init(q_taken, 2 + kSoftmaxWarps);  // the MMA warp, the V copy warp and the softmax warps
         mbar_init(q_empty, 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&k_full[i], 1);
@@ -163,6 +168,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
         mbar_init(o_done, 1);
         mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
+        mbar_init(d_full, 1);
         for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], kParts);
         mbar_fence_init();
     }
@@ -182,15 +188,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
     const uint32_t tm = *tmem_slot;
 
     if (warp == kProducerWarp) {
-        // ------------------------------ producer ------------------------------
+        // ---------------------- item, Q and K copy warp ----------------------
         if (lane == 0) {
             tma_prefetch_desc(&kv_map);
             tma_prefetch_desc(&q_map);
         }
-        const int Hkv = a.num_kv_heads;
         constexpr int kTileBlocks = kChunkKeys / PKV_BLOCK_SIZE;  // 8 blocks per key tile
-        uint32_t jt = 0;  // K/V tiles of the items so far
-        uint32_t k_issued = 0, v_issued = 0;
+        uint32_t jt = 0;  // K tiles of the items so far
+        uint32_t k_issued = 0;
         bool ok = true;
         // Global reads that a load depends on are issued ahead of it: the
         // next item is claimed while the current one issues its last K tile,
@@ -222,6 +227,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
             if (it >= n_items) {
                 if (lane == 0) {
                     desc->item = -1;
+                    mbar_arrive(d_full);
                     mbar_arrive(q_full);
                 }
                 break;
@@ -231,6 +237,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                 d.item = it; d.r = r; d.mt = mt; d.h = h; d.q0 = q0; d.n = n; d.L = L; d.nv = nv;
                 d.kv_end = kv_end; d.nt = nt;
                 *desc = d;
+                mbar_arrive(d_full);
                 mbar_arrive_expect_tx(q_full, kChunkRows * D * 2);
 #pragma unroll
                 for (int bx = 0; bx < D / 64; ++bx)
@@ -238,41 +245,30 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
                                 q_full);
             }
             __syncwarp();
-            // K or V of key tile j into its ring slot: eight blocks, one box
-            // each.
-            auto load = [&](bool is_v, int j, int blk) {
+            // K of key tile j into its ring slot: eight blocks, one box each.
+            auto load = [&](int j, int blk) {
                 const uint32_t x = jt + j;
-                const int stages = is_v ? kVStages : kKStages;
-                const int st = x % stages;
-                uint64_t *full = is_v ? &v_full[st] : &k_full[st];
-                if (!mbar_wait(is_v ? &v_empty[st] : &k_empty[st], ((x / stages) & 1) ^ 1, status, abort))
-                    return false;
+                const int st = x % kKStages;
+                uint64_t *full = &k_full[st];
+                if (!mbar_wait(&k_empty[st], ((x / kKStages) & 1) ^ 1, status, abort)) return false;
                 if (blk < 0 || blk > a.num_blocks || (blk == a.num_blocks && j * kTileBlocks + lane < kvb)) {
                     if (lane < kTileBlocks) raise_status(status, PKV_DEV_BAD_BLOCK);
                     blk = a.num_blocks;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(full, kChunkKeys * D * 2);
                 __syncwarp();
-                if (lane < kTileBlocks) {
-                    uint8_t *dst = smem + (is_v ? S::kOffV : S::kOffK) + st * S::kTile + lane * S::kBlk;
-                    tma_load_5d(dst, &kv_map, 0, 0, 0, (is_v ? Hkv + h : h) * 2, blk, full);
-                }
+                if (lane < kTileBlocks)
+                    tma_load_5d(smem + S::kOffK + st * S::kTile + lane * S::kBlk, &kv_map, 0, 0, 0, h * 2, blk, full);
                 __syncwarp();
-                if (is_v) ++v_issued; else ++k_issued;
+                ++k_issued;
                 return true;
             };
             auto claim_next = [&]() {
                 if (lane == 0) it_raw = atomicAdd(&a.header->next_chunk_item, 1);
             };
-            // K runs one tile ahead of V; V of tile j reuses K's block ids.
-            ok = load(false, 0, id0);
-            if (nt == 1) claim_next();
             for (int j = 0; j < nt && ok; ++j) {
-                if (j + 1 < nt) {
-                    ok = load(false, j + 1, id1);
-                    if (j + 2 == nt) claim_next();
-                }
-                if (ok) ok = load(true, j, id0);
+                ok = load(j, id0);
+                if (j + 1 == nt) claim_next();
                 id0 = id1;
                 id1 = id2;
                 id2 = fetch(j + 3);
@@ -285,6 +281,51 @@ chunk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__
             // let copies already issued land before the CTA can leave
             for (uint32_t x = k_issued > (uint32_t)kKStages ? k_issued - kKStages : 0; x < k_issued; ++x)
                 mbar_drain(&k_full[x % kKStages], (x / kKStages) & 1, status, diag, 0x2);
+        }
+    } else if (warp == kVWarp) {
+        // ---------------------------- V copy warp ----------------------------
+        // Takes each item from desc (d_full) and copies its V tiles, one box
+        // per block, into the V ring; block ids read three tiles ahead.
+        const int Hkv = a.num_kv_heads;
+        constexpr int kTileBlocks = kChunkKeys / PKV_BLOCK_SIZE;
+        uint32_t jt = 0, v_issued = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            if (!warp_wait(d_full, k & 1, status, abort)) { ok = false; break; }
+            const ChunkDesc d = *desc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_taken);
+            if (d.item < 0) break;
+            const int nt = d.nt;
+            const int kvb = (d.kv_end + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+            const int32_t *bt = a.block_table + (long long)d.r * a.max_blocks_per_req;
+            auto fetch = [&](int t) {
+                const int kb = t * kTileBlocks + lane;
+                return (lane < kTileBlocks && t < nt && kb < kvb) ? __ldg(bt + kb) : a.num_blocks;
+            };
+            int id0 = fetch(0), id1 = fetch(1), id2 = fetch(2);
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t x = jt + j;
+                const int st = x % kVStages;
+                if (!warp_wait(&v_empty[st], ((x / kVStages) & 1) ^ 1, status, abort)) { ok = false; break; }
+                int blk = id0;  // a bad id was reported by the K copy warp; TMA fills zeros for it here
+                if (blk < 0 || blk > a.num_blocks || (blk == a.num_blocks && j * kTileBlocks + lane < kvb))
+                    blk = a.num_blocks;
+                if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kChunkKeys * D * 2);
+                __syncwarp();
+                if (lane < kTileBlocks)
+                    tma_load_5d(smem + S::kOffV + st * S::kTile + lane * S::kBlk, &kv_map, 0, 0, 0, (Hkv + d.h) * 2,
+                                blk, &v_full[st]);
+                __syncwarp();
+                ++v_issued;
+                id0 = id1;
+                id1 = id2;
+                id2 = fetch(j + 3);
+            }
+            jt += nt;
+        }
+        if (!ok && lane == 0) {
+            // let copies already issued land before the CTA can leave
             for (uint32_t x = v_issued > (uint32_t)kVStages ? v_issued - kVStages : 0; x < v_issued; ++x)
                 mbar_drain(&v_full[x % kVStages], (x / kVStages) & 1, status, diag, 0x2);
         }
