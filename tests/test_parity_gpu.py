@@ -209,6 +209,25 @@ def test_bad_metadata_raises_status_without_fault():
     assert st & pkv.PKV_DEV_BAD_LEN and wst & pkv.PKV_DEV_BAD_LEN
 
 
+@pytest.mark.parametrize("shape", [TINY, LLAMA], ids=["d64", "d128"])
+def test_chunk_tile_bad_block_is_reported_and_zero_filled(shape):
+    """A block id past the pool in a chunk-tile request's table (block 8, the
+    first of the second key tile): the chunk kernel's copy warps report
+    PKV_DEV_BAD_BLOCK and copy zeros in its place; the rows that never see
+    that block (tokens 0-127) and the other request still match the oracle."""
+    batch = _custom(shape, [512, 300], [512, 1], 112)
+    ten = device_tensors(batch, generate_on="cpu")
+    _, _, ref = oracle_step(batch, host_inputs(ten))
+    bad = wl.Batch(**{**batch.__dict__})
+    bad.block_table = batch.block_table.copy()
+    bad.block_table[0, 8] = batch.num_blocks + 7
+    buf, st, wst = run_gpu_step(bad, {k: v.clone() for k, v in ten.items()})
+    assert wst & pkv.PKV_DEV_BAD_BLOCK
+    assert torch.isfinite(buf.out.float()).all()
+    keep = list(range(128)) + [512]  # request 0's first 128 tokens, request 1's token
+    assert_attention_close(buf.out[keep], ref[keep], what="rows without the bad block")
+
+
 def test_empty_batch_is_a_no_op():
     q = torch.empty(0, 32, 128, dtype=torch.bfloat16, device="cuda")
     pool = torch.zeros(4, 2, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
