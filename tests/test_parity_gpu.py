@@ -228,6 +228,23 @@ def test_chunk_tile_bad_block_is_reported_and_zero_filled(shape):
     assert_attention_close(buf.out[keep], ref[keep], what="rows without the bad block")
 
 
+@pytest.mark.parametrize("workload", ["mixed", "tinyllama"])
+def test_repeated_steps_give_the_same_bits(workload):
+    """Back-to-back steps on the same inputs (the pipelined launches, the
+    chunk kernel beside the split-KV kernel, dynamic work claims) leave clean
+    status words and bit-identical outputs every time: a race between the
+    kernels' roles would show up as a changed bit or a timeout."""
+    batch = wl.make_batch(workload)
+    buf = pkv.StepBuffers(batch, device_tensors(batch))
+    first = buf.step().clone()
+    for i in range(400):
+        out = buf.step()
+        if i % 100 == 99:
+            torch.cuda.synchronize()
+            assert pkv.pkv_read_status(buf.status) == 0 and pkv.pkv_read_status(buf.workspace) == 0
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"step {i + 1}"
+
+
 def test_empty_batch_is_a_no_op():
     q = torch.empty(0, 32, 128, dtype=torch.bfloat16, device="cuda")
     pool = torch.zeros(4, 2, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
